@@ -1,0 +1,178 @@
+/*
+ * gbtopk — batched variable-length exact top-K for the sparse-attention
+ * (DSA) indexer decode step, on NVIDIA GB300 (sm_103a).
+ *
+ * C ABI.  Every pointer argument is a plain pointer; "device" means it must
+ * point into CUDA device memory (or managed memory) of the current device,
+ * "host" means ordinary host memory.  All buffers are owned by the caller;
+ * the library allocates nothing, keeps no state between calls and never
+ * reads device data on the host, so every call can be captured in a CUDA
+ * graph and replayed with new seq_lens / lengths contents.
+ *
+ * Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ * default stream).  Host-side argument checks happen before anything is
+ * enqueued; a negative status means nothing was enqueued.
+ */
+#ifndef GBTOPK_H
+#define GBTOPK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types of the score matrix. */
+#define GBTOPK_F32 0  /* IEEE binary32 */
+#define GBTOPK_BF16 1 /* bfloat16 */
+#define GBTOPK_F16 2  /* IEEE binary16 */
+
+/* Status codes. */
+#define GBTOPK_OK 0
+#define GBTOPK_HINT_DISCARDED 1 /* warning: pre_idx unusable, ran hint-free (result still exact) */
+#define GBTOPK_EINVAL (-1)       /* shape, dtype, grouping or null-pointer error */
+#define GBTOPK_EALIGN (-2)       /* an output (or the score base) is misaligned */
+#define GBTOPK_EOVERLAP (-3)     /* two output buffers overlap */
+#define GBTOPK_EUNSUPPORTED (-4) /* outside the supported envelope (e.g. top_k too large) */
+#define GBTOPK_ECUDA (-5)        /* the CUDA runtime refused the launch */
+#define GBTOPK_EWORKSPACE (-6)   /* workspace missing, misaligned or too small */
+#define GBTOPK_ETIMEOUT (-7)     /* device flag: a bounded wait gave up (see gbtopk_device_status) */
+
+/* Largest supported top_k. */
+#define GBTOPK_MAX_TOP_K 2048
+
+/*
+ * gbtopk_varlen — top-K over decode-step indexer logits.
+ *
+ * Defined by the FlashInfer `flashinfer.top_k_varlen` page (parameters
+ * logits, seq_lens, top_k, pre_idx, compress_ratio, next_n, return_values,
+ * out_indices, out_values; "returns") and the TensorRT-LLM PR #17821
+ * "self-sampling (GVR V2) top-K decode kernels" (exactness, MTP window,
+ * short-row and value-padding conventions).
+ *
+ *  logits       device, [num_rows, width] of `dtype`, inner stride 1, row
+ *               stride `row_stride` elements (>= width; arena views with a
+ *               padded stride are accepted).  Must be aligned to the element
+ *               size.  Columns at or beyond a row's valid count are never read.
+ *  seq_lens     device int32 [num_rows / next_n]: KV-token lengths.  Row r
+ *               (request i = r / next_n, t = r % next_n) ranks its first
+ *               n_r = max(0, (seq_lens[i] - next_n + t + 1) / compress_ratio)
+ *               columns, clamped to `width`.
+ *  next_n       >= 1, and num_rows % next_n == 0.
+ *  compress_ratio >= 1.
+ *  top_k        1 .. GBTOPK_MAX_TOP_K.
+ *  pre_idx      device int32 [num_rows / next_n, top_k] or NULL: the previous
+ *               step's top-K columns of each request, raw (no +1 offset),
+ *               pre_idx[i][0] the argmax.  It only steers the threshold guess
+ *               and never changes the result.  Entries outside [0, n_r)
+ *               (including -1) and duplicates are ignored.  A pointer that
+ *               is not 16-byte aligned is discarded with status
+ *               GBTOPK_HINT_DISCARDED.
+ *  out_indices  device int32 [num_rows, top_k], 16-byte aligned.  Row r gets
+ *               min(top_k, n_r) column indices followed by -1.
+ *  out_values   device, dtype of logits, [num_rows, top_k], 16-byte aligned,
+ *               or NULL.  Selected values are bit copies; padding slots hold
+ *               the lowest finite value of the dtype.
+ *  deterministic  0: ties at the k-th value are resolved arbitrarily and the
+ *               selected columns come in no particular order.  1: ties take
+ *               the smallest columns and each row is ordered by (value
+ *               descending, column ascending).  Short rows (n_r <= top_k)
+ *               come in column order when 0.
+ *  workspace    device scratch of at least gbtopk_workspace_bytes(...) bytes,
+ *               256-byte aligned, zero-filled before its first use.  Every
+ *               call leaves it zero-filled again.  Calls that may overlap in
+ *               time (different streams, concurrent graph replays) need
+ *               separate workspaces.
+ *  stream       cudaStream_t.
+ *
+ * Returns GBTOPK_OK / GBTOPK_HINT_DISCARDED, or a negative status (nothing
+ * enqueued).  num_rows == 0 is a no-op.
+ */
+int gbtopk_varlen(const void *logits, int dtype, int64_t num_rows, int64_t width,
+                  int64_t row_stride, const int32_t *seq_lens, int32_t next_n,
+                  int32_t compress_ratio, int32_t top_k, const int32_t *pre_idx,
+                  int32_t *out_indices, void *out_values, int deterministic,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * gbtopk_page_table_transform — top-K fused with the compact page-table
+ * transform.
+ *
+ * Defined by the FlashInfer compact page-table PR body quoted on the SGLang
+ * PR #33237 page ("--dsa-topk-backend flashinfer with fused top-k"): for a
+ * selected local score index idx,
+ *     page = page_table[r, pt_row_start_r + idx / page_size]
+ *     out  = page * page_size + idx % page_size,     out_raw = idx,
+ * with -1 padding kept in both outputs, which stay positionally aligned.
+ *
+ *  scores       device, [num_rows, width] of `dtype`, inner stride 1, row
+ *               stride `row_stride` elements.
+ *  lengths      device int32 [num_rows]: valid scores per row.
+ *  row_starts   device int32 [num_rows] or NULL: offset of the row's first
+ *               valid score, in score elements.  The valid window is
+ *               [row_start, row_start + length) clamped to the width; a
+ *               row_start outside [0, width] gives an empty row.  Indices
+ *               are local to row_start.
+ *  page_table   device int32 [num_rows, pt_cols], inner stride 1, row stride
+ *               pt_row_stride entries (non-contiguous tables are accepted).
+ *  pt_row_starts  device int32 [num_rows] or NULL: first page-table entry of
+ *               each row, in page-table entries.  NULL means row_starts when
+ *               page_size == 1 and 0 when row_starts is NULL; NULL together
+ *               with row_starts and page_size > 1 is GBTOPK_EINVAL.
+ *  page_size    1 .. 2^30.  A page-table column outside [0, pt_cols) yields
+ *               -1 in `out` (out_raw still holds idx).  page * page_size +
+ *               idx % page_size is computed modulo 2^32: keeping it inside
+ *               int32 is the caller's responsibility.
+ *  top_k        1 .. GBTOPK_MAX_TOP_K.
+ *  out          device int32 [num_rows, top_k], 16-byte aligned.
+ *  out_raw      device int32 [num_rows, top_k], 16-byte aligned, or NULL; must
+ *               not overlap `out` (GBTOPK_EOVERLAP).
+ *  deterministic, workspace, stream: as for gbtopk_varlen.
+ */
+int gbtopk_page_table_transform(const void *scores, int dtype, int64_t num_rows,
+                                int64_t width, int64_t row_stride,
+                                const int32_t *lengths, const int32_t *row_starts,
+                                const int32_t *page_table, int64_t pt_cols,
+                                int64_t pt_row_stride, const int32_t *pt_row_starts,
+                                int32_t page_size, int32_t top_k, int32_t *out,
+                                int32_t *out_raw, int deterministic, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
+/*
+ * gbtopk_workspace_bytes — scratch needed by a call with this geometry.
+ * A pure function of its arguments (capture-stable).  The workspace holds a
+ * device status word plus, when rows are long enough to be split across
+ * thread blocks, per-row candidate buffers, counters and histograms (the
+ * multi-CTA split described on the FlashInfer `top_k_varlen` page, parameter
+ * `workspace`).  Returns 0 for invalid arguments.
+ */
+size_t gbtopk_workspace_bytes(int64_t num_rows, int64_t width, int32_t top_k, int dtype);
+
+/*
+ * gbtopk_device_status — reads (and clears) the device status word of a
+ * workspace.  Synchronises `stream`.  *flags receives a bit set: bit 0 = a
+ * bounded wait on an asynchronous copy gave up (the affected rows were then
+ * recomputed from global memory, so outputs stay exact).  Returns GBTOPK_OK,
+ * GBTOPK_EINVAL or GBTOPK_ECUDA.
+ */
+int gbtopk_device_status(void *workspace, uint32_t *flags, void *stream);
+
+/*
+ * gbtopk_plan_query — the launch plan for a geometry, for inspection and
+ * tests.  Fills out[0..7] = {chunk elements per block, chunks per row,
+ * threads per block, dynamic shared memory bytes, split (0/1), candidate
+ * capacity per split row, grid size, workspace bytes}.  Returns GBTOPK_OK or
+ * GBTOPK_EINVAL / GBTOPK_EUNSUPPORTED.
+ */
+int gbtopk_plan_query(int64_t num_rows, int64_t width, int32_t top_k, int dtype,
+                      int64_t *out);
+
+/* Human-readable name of a status code (static string). */
+const char *gbtopk_status_str(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBTOPK_H */
