@@ -51,6 +51,9 @@ def parse():
                     default="dsv32_decode")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="short run for profilers: warm-up + K steps, no clock sampling, "
+                         "no e2e and no CPU leg")
     return ap.parse_args()
 
 
@@ -267,6 +270,14 @@ def run_gbtopk(args, rank, world, local):
     for i in range(max(args.warmup, 3)):
         step(i)
     torch.cuda.synchronize(dev)
+    if args.profile:
+        for s in range(args.steps):
+            step(s)
+        torch.cuda.synchronize(dev)
+        if rank == 0:
+            print(json.dumps({"profile_run": True, "steps": args.steps, "rows": R, "width": W,
+                              "algorithmic_bytes_per_launch": algo_bytes}), flush=True)
+        return
 
     # keep the GPU busy ~1 s around the timed region so the clock samples
     # reflect it, then time exactly K steps

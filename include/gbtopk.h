@@ -80,10 +80,13 @@ extern "C" {
  *               descending, column ascending).  Short rows (n_r <= top_k)
  *               come in column order when 0.
  *  workspace    device scratch of at least gbtopk_workspace_bytes(...) bytes,
- *               256-byte aligned, zero-filled before its first use.  Every
- *               call leaves it zero-filled again.  Calls that may overlap in
- *               time (different streams, concurrent graph replays) need
- *               separate workspaces.
+ *               256-byte aligned, zero-filled before its first use.  Its
+ *               layout is the same for every geometry: a status word, then
+ *               per row a block of counters and a histogram that every call
+ *               leaves zero-filled again, followed by candidate scratch.  So
+ *               one workspace, zeroed once, serves any sequence of calls on
+ *               one stream.  Calls that may overlap in time (different
+ *               streams, concurrent graph replays) need separate workspaces.
  *  stream       cudaStream_t.
  *
  * Returns GBTOPK_OK / GBTOPK_HINT_DISCARDED, or a negative status (nothing
@@ -160,9 +163,10 @@ int gbtopk_device_status(void *workspace, uint32_t *flags, void *stream);
 
 /*
  * gbtopk_plan_query — the launch plan for a geometry, for inspection and
- * tests.  Fills out[0..7] = {chunk elements per block, chunks per row,
+ * tests.  Fills out[0..9] = {chunk elements per block, chunks per row,
  * threads per block, dynamic shared memory bytes, split (0/1), candidate
- * capacity per split row, grid size, workspace bytes}.  Returns GBTOPK_OK or
+ * capacity per split row, grid size, workspace bytes, workspace bytes per
+ * split row, leading bytes of each row block kept zero between calls}.  Returns GBTOPK_OK or
  * GBTOPK_EINVAL / GBTOPK_EUNSUPPORTED.
  */
 int gbtopk_plan_query(int64_t num_rows, int64_t width, int32_t top_k, int dtype,

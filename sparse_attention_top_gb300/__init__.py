@@ -106,10 +106,10 @@ def gbtopk_workspace_bytes(num_rows: int, width: int, top_k: int, dtype: torch.d
 
 
 def gbtopk_plan_query(num_rows: int, width: int, top_k: int, dtype: torch.dtype) -> dict:
-    out = (ctypes.c_int64 * 8)()
+    out = (ctypes.c_int64 * 10)()
     _check(load_library().gbtopk_plan_query(num_rows, width, top_k, _DTYPES[dtype], out))
     keys = ["chunk", "chunks_per_row", "threads", "smem_bytes", "split", "candidate_capacity",
-            "grid", "workspace_bytes"]
+            "grid", "workspace_bytes", "ws_row_bytes", "ws_row_counter_bytes"]
     return dict(zip(keys, list(out)))
 
 
@@ -155,8 +155,9 @@ def gbtopk_page_table_transform(scores: torch.Tensor, lengths: torch.Tensor,
 
 
 # One zero-filled workspace per (device, stream), grown on demand.  The
-# library leaves it zero-filled after every call.  Create it (by one eager
-# call) before capturing a CUDA graph on that stream.
+# library keeps its counters zero between calls and its layout does not
+# depend on the geometry, so one workspace serves every call on a stream.
+# Create it (by one eager call) before capturing a CUDA graph on that stream.
 _WS = {}
 
 

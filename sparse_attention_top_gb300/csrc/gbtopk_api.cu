@@ -49,7 +49,10 @@ int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *p
         pl.chunk = static_cast<int32_t>(chunk_max);
         pl.chunks_per_row = static_cast<int32_t>((width + chunk_max - 1) / chunk_max);
         pl.split = 1;
-        pl.gcap = 8 * top_k > 8192 ? 8 * top_k : 8192;
+        // Fixed per-row layout (independent of top_k, dtype and width) so one
+        // workspace serves every geometry: candidate scratch of one call can
+        // never land under another call's counters.
+        pl.gcap = gbtopk::kRowCandCap;
     }
     pl.grid = num_rows * pl.chunks_per_row;
     if (pl.grid > INT32_MAX) return GBTOPK_EUNSUPPORTED;
@@ -65,8 +68,7 @@ int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *p
     pl.off_u = align_up(pl.off_hist + hist, 16);
     pl.off_stage = align_up(pl.off_u + ureg, 16);
     pl.smem = pl.off_stage + stage;
-    pl.ws_row_bytes =
-        pl.split ? align_up(kRowHeaderBytes + 4 * kBins + 8 * static_cast<size_t>(pl.gcap), 256) : 0;
+    pl.ws_row_bytes = pl.split ? kRowBytes : 0;
     pl.ws_bytes = kWsHeaderBytes + static_cast<size_t>(num_rows) * pl.ws_row_bytes;
     *plan = pl;
     return GBTOPK_OK;
@@ -221,6 +223,8 @@ int gbtopk_plan_query(int64_t num_rows, int64_t width, int32_t top_k, int dtype,
     out[5] = plan.gcap;
     out[6] = plan.grid;
     out[7] = static_cast<int64_t>(plan.ws_bytes);
+    out[8] = static_cast<int64_t>(plan.ws_row_bytes);
+    out[9] = static_cast<int64_t>(gbtopk::kRowCounterBytes);
     return GBTOPK_OK;
 }
 

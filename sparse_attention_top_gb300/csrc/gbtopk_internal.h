@@ -17,6 +17,11 @@ constexpr int kLocalCap = 2048;        // candidates one block may publish
 constexpr int kChunkBytes = 32768;     // staged bytes per block for split rows
 constexpr size_t kWsHeaderBytes = 256; // device status word + padding
 constexpr int kRowHeaderBytes = 16;    // ticket, count, flags, pad
+constexpr int kRowCandCap = 16384;     // candidates per split row (8 x the largest top_k)
+// Per-row workspace of a split row: header + histogram (kept zero between
+// calls), then candidate scratch.
+constexpr size_t kRowCounterBytes = kRowHeaderBytes + 4 * kBins;
+constexpr size_t kRowBytes = (kRowCounterBytes + 8 * static_cast<size_t>(kRowCandCap) + 255) / 256 * 256;
 constexpr uint32_t kSpinLimit = 1u << 22;
 
 // Per-row flags in the split-row workspace.

@@ -251,7 +251,12 @@ def test_output_canaries_and_workspace_restored(dev):
         torch.cuda.synchronize(dev)
         assert bool((ibuf[:32] == canary).all()) and bool((ibuf[32 + R * k:] == canary).all())
         assert bool((vbuf[:32] == 1.25).all()) and bool((vbuf[32 + R * k:] == 1.25).all())
-        assert int(ws.count_nonzero()) == 0, "workspace not restored to zero"
+        plan = gb.gbtopk_plan_query(R, 70000, k, torch.float32)
+        rb, cb = plan["ws_row_bytes"], plan["ws_row_counter_bytes"]
+        assert int(ws[:256].count_nonzero()) == 0
+        for r in range(R):
+            blk = ws[256 + r * rb: 256 + r * rb + cb]
+            assert int(blk.count_nonzero()) == 0, f"row {r}: counters not restored to zero"
     n = _lengths(c)
     ref = _oracle_rows(c.logits, n, k, range(R))
     check_rows(c.logits, n, k, idx, ref, val)
