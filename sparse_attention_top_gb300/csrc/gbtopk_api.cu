@@ -56,17 +56,17 @@ int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *p
     }
     pl.grid = num_rows * pl.chunks_per_row;
     if (pl.grid > INT32_MAX) return GBTOPK_EUNSUPPORTED;
-    const size_t ctrl = 512;
-    const size_t hist = 4 * static_cast<size_t>(pl.split ? kBins : 256);
-    size_t ureg = static_cast<size_t>(sel_cap) * 8;
-    if (pl.split) {
-        ureg = ureg > static_cast<size_t>(kSampleSize) * 4 ? ureg : static_cast<size_t>(kSampleSize) * 4;
-        ureg = ureg > static_cast<size_t>(kLocalCap) * 8 ? ureg : static_cast<size_t>(kLocalCap) * 8;
+    // Shared memory: control block | histogram (kBins counters; also the
+    // row sample and, once the histogram is consumed, the selection buffer)
+    // | staged chunk (also candidate / boundary-bin scratch).
+    size_t hist = static_cast<size_t>(sel_cap) * 8;
+    if (pl.split || width > kExactMax) {
+        hist = hist > static_cast<size_t>(kBins) * 4 ? hist : static_cast<size_t>(kBins) * 4;
+        hist = hist > static_cast<size_t>(kSampleSize) * 4 ? hist : static_cast<size_t>(kSampleSize) * 4;
     }
     const size_t stage = align_up((static_cast<size_t>(pl.chunk) + 16 / es) * es, 16);
-    pl.off_hist = ctrl;
-    pl.off_u = align_up(pl.off_hist + hist, 16);
-    pl.off_stage = align_up(pl.off_u + ureg, 16);
+    pl.off_hist = kCtrlBytes;
+    pl.off_stage = align_up(pl.off_hist + hist, 16);
     pl.smem = pl.off_stage + stage;
     pl.ws_row_bytes = pl.split ? kRowBytes : 0;
     pl.ws_bytes = kWsHeaderBytes + static_cast<size_t>(num_rows) * pl.ws_row_bytes;

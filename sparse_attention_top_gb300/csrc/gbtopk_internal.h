@@ -12,11 +12,14 @@ namespace gbtopk {
 constexpr int kThreads = 256;          // threads per block
 constexpr int kSampleGroups = 256;     // one group of 8 consecutive columns per thread
 constexpr int kSampleSize = kSampleGroups * 8;
-constexpr int kBins = 1024;            // candidate histogram bins of a split row
-constexpr int kLocalCap = 2048;        // candidates one block may publish
+constexpr int kBinBits = 12;
+constexpr int kBins = 1 << kBinBits;   // candidate histogram bins
+constexpr int kRankMax = 256;          // boundary-bin size resolved by rank counting
+constexpr int kExactMax = 3072;        // rows up to this length: plain exact radix select
+constexpr size_t kCtrlBytes = 2048;    // per-block control block (counters, scan, digit histogram)
 constexpr int kChunkBytes = 32768;     // staged bytes per block for split rows
 constexpr size_t kWsHeaderBytes = 256; // device status word + padding
-constexpr int kRowHeaderBytes = 16;    // ticket, count, flags, pad
+constexpr int kRowHeaderBytes = 32;    // ticket, count, flags, t_lo, bin shift, pad
 constexpr int kRowCandCap = 16384;     // candidates per split row (8 x the largest top_k)
 // Per-row workspace of a split row: header + histogram (kept zero between
 // calls), then candidate scratch.
@@ -41,7 +44,7 @@ struct Plan {
     size_t ws_row_bytes;  // per-row workspace bytes (split plans)
     size_t ws_bytes;      // total workspace bytes
     // shared-memory layout (byte offsets)
-    size_t off_hist, off_u, off_stage;
+    size_t off_hist, off_stage;
 };
 
 // Kernel arguments.  Row-length source: varlen mode when seq_lens != null,

@@ -35,6 +35,26 @@
 #include "gbtopk_internal.h"
 
 namespace gbtopk {
+
+#ifdef GBTOPK_TRACE
+// Phase timestamps (%globaltimer, ns) of the first kTraceBlocks blocks, for
+// builds compiled with -DGBTOPK_TRACE (read back by gbtopk_trace_read).
+constexpr int kTraceBlocks = 1 << 16;
+__device__ unsigned long long g_trace[kTraceBlocks][8];
+#define GBTOPK_TRACE_POINT(slot, value)                                        \
+    do {                                                                       \
+        if (threadIdx.x == 0 && blockIdx.x < kTraceBlocks) {                   \
+            unsigned long long t_;                                             \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));             \
+            g_trace[blockIdx.x][slot] = (slot) == 7 ? (value) : t_;            \
+        }                                                                      \
+    } while (0)
+#else
+#define GBTOPK_TRACE_POINT(slot, value) \
+    do {                                \
+    } while (0)
+#endif
+
 namespace {
 
 // ---------------------------------------------------------------- keys
@@ -89,8 +109,9 @@ struct Ctrl {
     uint32_t key_max;
     uint32_t pad[3];
     uint32_t scan[72];
+    uint32_t rhist[256];     // radix-select digit histogram
 };
-static_assert(sizeof(Ctrl) <= 512, "control block");
+static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
 // ---------------------------------------------------------------- small helpers
 
@@ -196,10 +217,13 @@ __device__ __forceinline__ uint32_t ldg_raw(const R *p) {
 }
 
 // ---------------------------------------------------------------- key sources
-// A source yields (key, column index, raw bits) for item i.
+// A source yields (key, column index, raw bits) for item i.  kBatch items
+// per thread are fetched before any is used, so global-memory sources keep
+// several loads in flight per thread.
 
 template <int DT>
 struct StageSrc {  // a row (or chunk) staged in shared memory
+    static constexpr int kBatch = 4;
     const typename Elem<DT>::raw_t *s;
     __device__ __forceinline__ void get(int64_t i, uint32_t &key, uint32_t &idx, uint32_t &raw) const {
         raw = s[i];
@@ -210,6 +234,7 @@ struct StageSrc {  // a row (or chunk) staged in shared memory
 
 template <int DT>
 struct GlobalSrc {  // a row read straight from global memory
+    static constexpr int kBatch = 8;
     const typename Elem<DT>::raw_t *g;
     __device__ __forceinline__ void get(int64_t i, uint32_t &key, uint32_t &idx, uint32_t &raw) const {
         raw = ldg_raw(g + i);
@@ -220,6 +245,7 @@ struct GlobalSrc {  // a row read straight from global memory
 
 template <int DT>
 struct PairSrc {  // (raw, column) pairs in shared memory
+    static constexpr int kBatch = 4;
     const uint2 *p;
     __device__ __forceinline__ void get(int64_t i, uint32_t &key, uint32_t &idx, uint32_t &raw) const {
         const uint2 v = p[i];
@@ -229,7 +255,20 @@ struct PairSrc {  // (raw, column) pairs in shared memory
     }
 };
 
+template <int DT>
+struct GlobalPairSrc {  // (raw, column) pairs published by other blocks (read from L2)
+    static constexpr int kBatch = 8;
+    const uint2 *p;
+    __device__ __forceinline__ void get(int64_t i, uint32_t &key, uint32_t &idx, uint32_t &raw) const {
+        const uint2 v = __ldcg(p + i);
+        raw = v.x;
+        key = Elem<DT>::key(v.x);
+        idx = v.y;
+    }
+};
+
 struct KeyArraySrc {  // keys already mapped (the row sample)
+    static constexpr int kBatch = 8;
     const uint32_t *k;
     __device__ __forceinline__ void get(int64_t i, uint32_t &key, uint32_t &idx, uint32_t &raw) const {
         key = k[i];
@@ -238,57 +277,66 @@ struct KeyArraySrc {  // keys already mapped (the row sample)
     }
 };
 
-template <class S>
-struct ByKey {
-    S s;
-    __device__ __forceinline__ bool operator()(int64_t i, uint32_t &k) const {
-        uint32_t idx, raw;
-        s.get(i, k, idx, raw);
+// Visits items [0, cnt) of a source, kBatch per thread per pass, calling
+// f(valid, key, idx, raw) for each.  Every thread makes the same number of
+// calls (warp-collective operations inside f are allowed).
+template <class S, class F>
+__device__ __forceinline__ void for_each_item(const S &s, int64_t cnt, F &&f) {
+    constexpr int B = S::kBatch;
+    const int64_t step = static_cast<int64_t>(blockDim.x) * B;
+    for (int64_t base = 0; base < cnt; base += step) {
+        uint32_t key[B], idx[B], raw[B];
+        bool valid[B];
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            const int64_t i = base + static_cast<int64_t>(u) * blockDim.x + threadIdx.x;
+            valid[u] = i < cnt;
+            key[u] = idx[u] = raw[u] = 0;
+            if (valid[u]) s.get(i, key[u], idx[u], raw[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < B; ++u) f(valid[u], key[u], idx[u], raw[u]);
+    }
+}
+
+// Ranking modes for block_select: by key, or (deterministic ties) among the
+// items whose key equals t, smallest column first.
+struct RankByKey {
+    __device__ __forceinline__ bool operator()(uint32_t key, uint32_t, uint32_t &k) const {
+        k = key;
         return true;
     }
 };
 
-// Among items whose key equals `t`, ranks by smallest column first.
-template <class S>
-struct ByTieColumn {
-    S s;
+struct RankTieColumn {
     uint32_t t;
-    __device__ __forceinline__ bool operator()(int64_t i, uint32_t &k) const {
-        uint32_t key, idx, raw;
-        s.get(i, key, idx, raw);
+    __device__ __forceinline__ bool operator()(uint32_t key, uint32_t idx, uint32_t &k) const {
         k = ~idx;
         return key == t;
     }
 };
 
-// Block-wide radix select: the r-th largest (1-based) key among the valid
-// items of `src`, digit by digit from the top (8-bit digits, 256-bin shared
-// histogram).  With ROUNDS < KEY_BITS/8 the result is the r-th largest key
-// truncated to its top 8*ROUNDS bits (a lower bound of it).  Returns the key
-// and, in `gt`, how many valid items are strictly above it (exact when all
-// digits were resolved).  Requires 1 <= r <= number of valid items.
-template <int KEY_BITS, int ROUNDS, class Src>
-__device__ void block_select(const Src &src, int64_t cnt, uint32_t r, uint32_t *hist, Ctrl &c,
-                             uint32_t &out_key, uint32_t &out_gt) {
+// Block-wide radix select: the r-th largest (1-based) ranked value among the
+// items of `src` admitted by `mode`, digit by digit from the top (8-bit
+// digits, 256-bin shared histogram, warp-aggregated increments).  With
+// ROUNDS < KEY_BITS/8 the result is the r-th largest value truncated to its
+// top 8*ROUNDS bits (a lower bound of it).  Returns the value and, in `gt`,
+// how many admitted items rank strictly above it (exact when every digit
+// was resolved).  Requires 1 <= r <= number of admitted items.
+template <int KEY_BITS, int ROUNDS, class Src, class Mode>
+__device__ void block_select(const Src &src, const Mode &mode, int64_t cnt, uint32_t r,
+                             uint32_t *hist, Ctrl &c, uint32_t &out_key, uint32_t &out_gt) {
     uint32_t prefix = 0, mask = 0, rem = r;
 #pragma unroll 1
     for (int round = 0; round < ROUNDS; ++round) {
         const int shift = KEY_BITS - 8 * (round + 1);
         for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
         __syncthreads();
-        for (int64_t base = 0; base < cnt; base += blockDim.x) {
-            const int64_t i = base + threadIdx.x;
-            bool ok = false;
-            uint32_t d = 0;
-            if (i < cnt) {
-                uint32_t key;
-                if (src(i, key) && (key & mask) == prefix) {
-                    ok = true;
-                    d = (key >> shift) & 255u;
-                }
-            }
-            warp_hist_add(hist, d, ok);
-        }
+        for_each_item(src, cnt, [&](bool valid, uint32_t key, uint32_t idx, uint32_t) {
+            uint32_t k = 0;
+            const bool ok = valid && mode(key, idx, k) && (k & mask) == prefix;
+            warp_hist_add(hist, (k >> shift) & 255u, ok);
+        });
         __syncthreads();
         if (threadIdx.x < 32) {
             const uint32_t lane = lane_id();
@@ -346,18 +394,14 @@ __device__ void collect(const S &s, int64_t cnt, uint32_t t, uint32_t gt, uint32
         c.tie_count = 0;
     }
     __syncthreads();
-    for (int64_t b = 0; b < cnt; b += blockDim.x) {
-        const int64_t i = b + threadIdx.x;
-        uint32_t key = 0, idx = 0, raw = 0;
-        const bool valid = i < cnt;
-        if (valid) s.get(i, key, idx, raw);
+    for_each_item(s, cnt, [&](bool valid, uint32_t key, uint32_t idx, uint32_t raw) {
         const bool above = valid && key > t;
         const bool tie = valid && key == t && (!det || idx <= tie_col_max);
         const uint32_t slot = warp_claim(&c.sel_count, above);
         if (above) sel[base + slot] = make_uint2(raw, idx);
         const uint32_t tslot = warp_claim(&c.tie_count, tie);
         if (tie && tslot < need_ties) sel[base + gt + tslot] = make_uint2(raw, idx);
-    }
+    });
     __syncthreads();
 }
 
@@ -367,12 +411,12 @@ __device__ void exact_select(const S &s, int64_t n, int k, bool det, uint2 *sel,
                              Ctrl &c) {
     constexpr int KB = Elem<DT>::kKeyBits;
     uint32_t t, gt;
-    block_select<KB, KB / 8>(ByKey<S>{s}, n, static_cast<uint32_t>(k), hist, c, t, gt);
+    block_select<KB, KB / 8>(s, RankByKey{}, n, static_cast<uint32_t>(k), hist, c, t, gt);
     const uint32_t need_ties = static_cast<uint32_t>(k) - gt;
     uint32_t col_max = 0xFFFFFFFFu;
     if (det) {
         uint32_t kk, g2;
-        block_select<32, 4>(ByTieColumn<S>{s, t}, n, need_ties, hist, c, kk, g2);
+        block_select<32, 4>(s, RankTieColumn{t}, n, need_ties, hist, c, kk, g2);
         col_max = ~kk;
     }
     collect<DT>(s, n, t, gt, need_ties, det, col_max, sel, 0, c);
@@ -504,18 +548,278 @@ __device__ void drain_stage(Ctrl &c, uint32_t body_bytes, bool waited_ok) {
     if (threadIdx.x == 0 && body_bytes && !waited_ok) mbar_wait(&c.bar, 0);
 }
 
-// ---------------------------------------------------------------- the kernel
+// ---------------------------------------------------------------- threshold guess
 
+// From m sample keys in shared memory, the guess t_lo: the r-th largest
+// sample key truncated to its top 16 bits, with r chosen so that the count
+// of row elements >= t_lo falls below k only with a tiny probability
+// (r = e + 6 sqrt(e) + 2, e = m k / n the expected sample count at or above
+// the k-th largest).  Also the histogram scale: keys t_lo .. key_max map
+// onto the lower half of kBins bins.
+template <int DT>
+__device__ void guess_threshold(const uint32_t *sample, int m, int64_t n, int k, uint32_t key_max,
+                                Ctrl &c, uint32_t &t_lo, int &bin_shift) {
+    constexpr int KB = Elem<DT>::kKeyBits;
+    const double e = static_cast<double>(m) * k / static_cast<double>(n);
+    uint32_t r = static_cast<uint32_t>(ceil(e + 6.0 * sqrt(e) + 2.0));
+    if (r > static_cast<uint32_t>(m)) r = static_cast<uint32_t>(m);
+    uint32_t unused;
+    block_select<KB, 2>(KeyArraySrc{sample}, RankByKey{}, m, r, c.rhist, c, t_lo, unused);
+    const uint32_t range = key_max > t_lo ? key_max - t_lo : 0u;
+    const int bits = 32 - __clz(range);
+    bin_shift = bits > kBinBits - 1 ? bits - (kBinBits - 1) : 0;
+}
+
+// Element q of a 16-byte vector holding 4 (fp32) or 8 (16-bit) raw values,
+// without a dynamically indexed local array.
+template <int ES>
+__device__ __forceinline__ uint32_t vec_elem(const uint4 &w, int q) {
+    if (ES == 4) return q < 2 ? (q == 0 ? w.x : w.y) : (q == 2 ? w.z : w.w);
+    const int h = q >> 1;
+    const uint32_t word = h < 2 ? (h == 0 ? w.x : w.y) : (h == 2 ? w.z : w.w);
+    return (word >> (16 * (q & 1))) & 0xFFFFu;
+}
+
+__device__ __forceinline__ uint32_t bin_of(uint32_t key, uint32_t t_lo, int bin_shift) {
+    const uint32_t b = (key - t_lo) >> bin_shift;
+    return b < static_cast<uint32_t>(kBins - 1) ? b : static_cast<uint32_t>(kBins - 1);
+}
+
+// Keeps the staged elements whose key is >= t_lo.  Each thread first loads
+// its vectors into registers and marks passing elements in a bit mask; one
+// block scan then gives every thread its output slot, so candidates are
+// written without per-element atomics.  `reserve(total)` (thread 0) returns
+// the first slot; `put(slot, raw, col)` stores one candidate.  The key of
+// each candidate is also counted in hist (kBins bins).  Returns the number
+// of candidates of the chunk (block-uniform).
+template <int DT, class Reserve, class Put>
+__device__ uint32_t filter_chunk(const typename Elem<DT>::raw_t *stage, int off, int64_t len,
+                                 int64_t col_base, uint32_t t_lo, int bin_shift, uint32_t *hist,
+                                 Ctrl &c, Reserve &&reserve, Put &&put) {
+    constexpr int es = Elem<DT>::kBytes;
+    constexpr int EPV = 16 / es;
+    constexpr int VPT = (kChunkBytes + 16) / 16 / kThreads + 1;
+    const int64_t nvec = ((off + len) * es + 15) / 16;
+    const uint4 *svec = reinterpret_cast<const uint4 *>(stage);
+    uint4 w[VPT];
+    uint32_t msk[VPT];
+    uint32_t cnt = 0;
+    const float tf = __uint_as_float((t_lo & 0x80000000u) ? (t_lo & 0x7FFFFFFFu) : ~t_lo);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int64_t v = threadIdx.x + static_cast<int64_t>(j) * kThreads;
+        w[j] = v < nvec ? svec[v] : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int64_t v = threadIdx.x + static_cast<int64_t>(j) * kThreads;
+        // lanes of this vector that hold elements [0, len)
+        const int64_t e0 = v * EPV - off;
+        int lo = e0 < 0 ? static_cast<int>(-e0) : 0;
+        int hi = (len - e0) < EPV ? static_cast<int>(len - e0) : EPV;
+        uint32_t valid = 0;
+        if (v < nvec && hi > lo) valid = ((1u << hi) - 1u) & ~((1u << lo) - 1u);
+        uint32_t m = 0;
+#pragma unroll
+        for (int q = 0; q < EPV; ++q) {
+            const uint32_t raw = vec_elem<es>(w[j], q);
+            const bool pass = es == 4 ? __uint_as_float(raw) >= tf : Elem<DT>::key(raw) >= t_lo;
+            m |= static_cast<uint32_t>(pass) << q;
+        }
+        msk[j] = m & valid;
+        cnt += __popc(msk[j]);
+    }
+    uint32_t total;
+    const uint32_t excl = block_excl_scan(cnt, c, total);
+    if (threadIdx.x == 0) c.bcast[0] = reserve(total);
+    __syncthreads();
+    uint32_t slot = c.bcast[0] + excl;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        uint32_t m = msk[j];
+        const int64_t v = threadIdx.x + static_cast<int64_t>(j) * kThreads;
+        while (m) {
+            const int q = __ffs(m) - 1;
+            m &= m - 1;
+            const uint32_t raw = vec_elem<es>(w[j], q);
+            atomicAdd(&hist[bin_of(Elem<DT>::key(raw), t_lo, bin_shift)], 1u);
+            put(slot++, raw, static_cast<uint32_t>(col_base + v * EPV + q - off));
+        }
+    }
+    __syncthreads();
+    return total;
+}
+
+// Finds the exact top-k among `total` (>= k) candidates whose keys are
+// counted in hist[kBins] (shared memory): the bin b* holding the k-th key
+// from the top, every candidate of a higher bin, and the best `need` of bin
+// b* (ranked by key, then by smaller column).  Writes sel[0..k).  Returns
+// false when bin b* holds more candidates than `bcap` (caller falls back).
+// `sel` may alias `hist` (the histogram is consumed first).
+template <int DT, class CandSrc>
+__device__ bool select_from_candidates(const CandSrc &cands, uint32_t total, uint32_t *hist,
+                                       uint32_t t_lo, int bin_shift, int k, bool det, uint2 *sel,
+                                       uint2 *blist, uint32_t bcap, Ctrl &c) {
+    constexpr int BPT = kBins / kThreads;
+    constexpr int KB = Elem<DT>::kKeyBits;
+    uint32_t local[BPT], s = 0;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) {
+        local[j] = hist[kBins - 1 - BPT * threadIdx.x - j];
+        s += local[j];
+    }
+    uint32_t tot;
+    const uint32_t excl = block_excl_scan(s, c, tot);
+    if (excl < static_cast<uint32_t>(k) && static_cast<uint32_t>(k) <= excl + s) {
+        uint32_t acc = excl;
+#pragma unroll
+        for (int j = 0; j < BPT; ++j) {
+            if (acc + local[j] >= static_cast<uint32_t>(k)) {
+                c.bcast[2] = kBins - 1 - BPT * threadIdx.x - j;
+                c.bcast[3] = acc;
+                c.bcast[4] = local[j];
+                break;
+            }
+            acc += local[j];
+        }
+    }
+    if (threadIdx.x == 0) {
+        c.sel_count = 0;
+        c.b_count = 0;
+    }
+    __syncthreads();
+    const uint32_t bstar = c.bcast[2], above = c.bcast[3], bsize = c.bcast[4];
+    if (bsize > bcap) return false;
+    for_each_item(cands, total, [&](bool valid, uint32_t key, uint32_t idx, uint32_t raw) {
+        const uint32_t b = bin_of(key, t_lo, bin_shift);
+        const bool hi = valid && b > bstar;
+        const bool eq = valid && b == bstar;
+        const uint32_t slot = warp_claim(&c.sel_count, hi);
+        if (hi) sel[slot] = make_uint2(raw, idx);
+        const uint32_t bslot = warp_claim(&c.b_count, eq);
+        if (eq) blist[bslot] = make_uint2(raw, idx);
+    });
+    __syncthreads();
+    const uint32_t need = static_cast<uint32_t>(k) - above;
+    if (bsize <= kRankMax) {
+        // rank every member of bin b* against the others: a total order by
+        // (key desc, column asc); the first `need` ranks are selected
+        for (uint32_t i = threadIdx.x; i < bsize; i += blockDim.x) {
+            const uint2 me = blist[i];
+            const uint32_t mk = Elem<DT>::key(me.x);
+            uint32_t rank = 0;
+            for (uint32_t j = 0; j < bsize; ++j) {
+                const uint2 o = blist[j];
+                const uint32_t ok = Elem<DT>::key(o.x);
+                rank += (ok > mk || (ok == mk && o.y < me.y)) ? 1u : 0u;
+            }
+            if (rank < need) sel[above + rank] = me;
+        }
+        __syncthreads();
+    } else {
+        const PairSrc<DT> bs{blist};
+        uint32_t t, gt;
+        block_select<KB, KB / 8>(bs, RankByKey{}, bsize, need, c.rhist, c, t, gt);
+        const uint32_t need_ties = need - gt;
+        uint32_t col_max = 0xFFFFFFFFu;
+        if (det) {
+            uint32_t kk, g2;
+            block_select<32, 4>(bs, RankTieColumn{t}, bsize, need_ties, c.rhist, c, kk, g2);
+            col_max = ~kk;
+        }
+        collect<DT>(bs, bsize, t, gt, need_ties, det, col_max, sel, above, c);
+    }
+    return true;
+}
+
+// Samples m keys of a row staged in shared memory (single elements at a
+// fixed stride) into `sample`, and their maximum into c.key_max.
+template <int DT>
+__device__ void sample_staged(const typename Elem<DT>::raw_t *row, int64_t n, int m, uint32_t *sample,
+                              Ctrl &c) {
+    if (threadIdx.x == 0) c.key_max = 0;
+    __syncthreads();
+    uint32_t kmax = 0;
+    for (int i = threadIdx.x; i < m; i += blockDim.x) {
+        const uint32_t key = Elem<DT>::key(row[static_cast<int64_t>(i) * n / m]);
+        sample[i] = key;
+        kmax = key > kmax ? key : kmax;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const uint32_t y = __shfl_xor_sync(0xffffffffu, kmax, o);
+        kmax = y > kmax ? y : kmax;
+    }
+    if (lane_id() == 0) atomicMax(&c.key_max, kmax);
+    __syncthreads();
+}
+
+// ---------------------------------------------------------------- kernels
+
+// Guess kernel: one block per split row computes the row's threshold guess
+// from a strided sample (256 groups of 8 consecutive columns), anchored at
+// the hint's argmax column when a hint is given, and stores it in the row's
+// workspace header.  It lets the main kernel launch at once (programmatic
+// dependent launch), so the main kernel's bulk copies overlap this work.
+template <int DT>
+__global__ void __launch_bounds__(kThreads) guess_kernel(const __grid_constant__ Params p) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __shared__ Ctrl c;
+    __shared__ uint32_t sample[kSampleSize];
+    const int64_t row = blockIdx.x;
+    int64_t n, col0;
+    row_window(p, row, n, col0);
+    if (n <= p.k || n <= p.plan.chunk) return;
+    const typename Elem<DT>::raw_t *xrow =
+        static_cast<const typename Elem<DT>::raw_t *>(p.x) + row * p.row_stride + col0;
+    if (threadIdx.x == 0) c.key_max = 0;
+    const int64_t pos = static_cast<int64_t>(threadIdx.x) * (n - 8) / (kSampleGroups - 1);
+    uint32_t kmax = 0;
+    uint32_t raw[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) raw[j] = ldg_raw(xrow + pos + j);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t key = Elem<DT>::key(raw[j]);
+        sample[threadIdx.x * 8 + j] = key;
+        kmax = key > kmax ? key : kmax;
+    }
+    if (threadIdx.x == 0 && p.pre_idx) {  // hint anchor: previous argmax
+        const int32_t a = __ldg(p.pre_idx + (row / p.next_n) * p.k);
+        if (static_cast<uint64_t>(static_cast<uint32_t>(a)) < static_cast<uint64_t>(n)) {
+            const uint32_t key = Elem<DT>::key(ldg_raw(xrow + a));
+            kmax = key > kmax ? key : kmax;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const uint32_t y = __shfl_xor_sync(0xffffffffu, kmax, o);
+        kmax = y > kmax ? y : kmax;
+    }
+    __syncthreads();
+    if (lane_id() == 0) atomicMax(&c.key_max, kmax);
+    __syncthreads();
+    uint32_t t_lo;
+    int bin_shift;
+    guess_threshold<DT>(sample, kSampleSize, n, p.k, c.key_max, c, t_lo, bin_shift);
+    if (threadIdx.x == 0) {
+        uint32_t *rhdr = reinterpret_cast<uint32_t *>(p.ws + kWsHeaderBytes +
+                                                      static_cast<size_t>(row) * p.plan.ws_row_bytes);
+        rhdr[3] = t_lo;
+        rhdr[4] = static_cast<uint32_t>(bin_shift);
+    }
+}
+
+// Main kernel: block b handles chunk b % C of row b / C.
 template <int DT>
 __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ Params p) {
     using raw_t = typename Elem<DT>::raw_t;
-    constexpr int KB = Elem<DT>::kKeyBits;
     extern __shared__ __align__(128) uint8_t smem[];
     Ctrl &c = *reinterpret_cast<Ctrl *>(smem);
     uint32_t *hist = reinterpret_cast<uint32_t *>(smem + p.plan.off_hist);
-    uint8_t *ureg = smem + p.plan.off_u;
+    uint2 *sel = reinterpret_cast<uint2 *>(smem + p.plan.off_hist);  // aliases hist
     raw_t *stage = reinterpret_cast<raw_t *>(smem + p.plan.off_stage);
-    uint2 *sel = reinterpret_cast<uint2 *>(ureg);
+    const uint32_t stage_pairs = static_cast<uint32_t>((p.plan.smem - p.plan.off_stage) / sizeof(uint2));
 
     const int cpr = p.plan.chunks_per_row;
     const int64_t row = static_cast<int64_t>(blockIdx.x) / cpr;
@@ -523,12 +827,15 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
     const int k = p.k;
     const bool det = p.deterministic != 0;
 
+    GBTOPK_TRACE_POINT(0, 0);
     int64_t n, col0;
     row_window(p, row, n, col0);
+    GBTOPK_TRACE_POINT(1, 0);
     const raw_t *xrow = static_cast<const raw_t *>(p.x) + row * p.row_stride + col0;
 
     // ---- short and empty rows: every valid column, then -1
     if (n <= k) {
+        GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | (chunk ? 0u : 1u));
         if (chunk != 0) return;
         const bool need_raw = det || p.out_val != nullptr;
         for (int j = threadIdx.x; j < n; j += blockDim.x)
@@ -536,27 +843,59 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
         __syncthreads();
         if (det) sort_selection<DT>(sel, static_cast<int>(n));
         emit<DT>(p, row, sel, static_cast<int>(n));
+        GBTOPK_TRACE_POINT(6, 0);
         return;
     }
 
     const int64_t CH = p.plan.chunk;
     const int64_t nch = (n + CH - 1) / CH;
-    if (chunk >= nch) return;
+    if (chunk >= nch) {
+        GBTOPK_TRACE_POINT(7, static_cast<unsigned long long>(n) << 8);
+        return;
+    }
 
     if (threadIdx.x == 0) mbar_init(&c.bar);
     __syncthreads();
 
-    // ---- single-chunk rows: exact select on the staged row
+    // ---- single-chunk rows: everything in shared memory
     if (nch == 1) {
         int off;
         const uint32_t body = stage_row<DT>(xrow, n, stage, &c.bar, off);
         __syncthreads();
         const bool ok = wait_stage(p, c, body);
-        if (ok) exact_select<DT>(StageSrc<DT>{stage + off}, n, k, det, sel, hist, c);
-        else exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, det, sel, hist, c);
+        GBTOPK_TRACE_POINT(3, 0);
+        bool done = false;
+        if (ok && n > kExactMax) {
+            // sampled guess from the staged row, filter, exact select
+            uint32_t *sample = hist;  // dead before the histogram is built
+            sample_staged<DT>(stage + off, n, kSampleSize, sample, c);
+            uint32_t t_lo;
+            int bin_shift;
+            guess_threshold<DT>(sample, kSampleSize, n, k, c.key_max, c, t_lo, bin_shift);
+            for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
+            __syncthreads();
+            uint2 *lcand = reinterpret_cast<uint2 *>(stage);  // rows are in registers by then
+            const uint32_t total = filter_chunk<DT>(
+                stage, off, n, 0, t_lo, bin_shift, hist, c, [](uint32_t) { return 0u; },
+                [&](uint32_t slot, uint32_t raw, uint32_t col) {
+                    if (slot < stage_pairs) lcand[slot] = make_uint2(raw, col);
+                });
+            if (total >= static_cast<uint32_t>(k) && total <= stage_pairs) {
+                done = select_from_candidates<DT>(PairSrc<DT>{lcand}, total, hist, t_lo, bin_shift, k,
+                                                  det, sel, lcand + total, stage_pairs - total, c);
+            }
+            if (!done) exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, det, sel, c.rhist, c);
+            done = true;
+        }
+        if (!done) {
+            if (ok) exact_select<DT>(StageSrc<DT>{stage + off}, n, k, det, sel, c.rhist, c);
+            else exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, det, sel, c.rhist, c);
+        }
         if (det) sort_selection<DT>(sel, k);
         emit<DT>(p, row, sel, k);
         drain_stage(c, body, ok);
+        GBTOPK_TRACE_POINT(6, 0);
+        GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | 2u);
         return;
     }
 
@@ -565,105 +904,38 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
     const int64_t len = (n - c0) < CH ? (n - c0) : CH;
     int off;
     const uint32_t body = stage_row<DT>(xrow + c0, len, stage, &c.bar, off);
-
-    // Self-sampling guess: 256 groups of 8 consecutive columns spread over
-    // the row; the same positions in every block of the row.
-    uint32_t *sample = reinterpret_cast<uint32_t *>(ureg);
-    if (threadIdx.x == 0) c.key_max = 0;
-    {
-        const int64_t pos = static_cast<int64_t>(threadIdx.x) * (n - 8) / (kSampleGroups - 1);
-        uint32_t kmax = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint32_t key = Elem<DT>::key(ldg_raw(xrow + pos + j));
-            sample[threadIdx.x * 8 + j] = key;
-            kmax = key > kmax ? key : kmax;
-        }
-        if (threadIdx.x == 0 && p.pre_idx) {  // hint anchor: previous argmax
-            const int32_t a = __ldg(p.pre_idx + (row / p.next_n) * k);
-            if (static_cast<uint32_t>(a) < static_cast<uint64_t>(n)) {
-                const uint32_t key = Elem<DT>::key(ldg_raw(xrow + a));
-                kmax = key > kmax ? key : kmax;
-            }
-        }
-#pragma unroll
-        for (int off2 = 16; off2 > 0; off2 >>= 1) {
-            const uint32_t y = __shfl_xor_sync(0xffffffffu, kmax, off2);
-            kmax = y > kmax ? y : kmax;
-        }
-        __syncthreads();
-        if (lane_id() == 0) atomicMax(&c.key_max, kmax);
-    }
-    __syncthreads();
-    const double e = static_cast<double>(kSampleSize) * k / static_cast<double>(n);
-    uint32_t r_lo = static_cast<uint32_t>(ceil(e + 6.0 * sqrt(e) + 2.0));
-    if (r_lo > static_cast<uint32_t>(kSampleSize)) r_lo = kSampleSize;
-    uint32_t t_lo, unused;
-    block_select<KB, 2>(ByKey<KeyArraySrc>{KeyArraySrc{sample}}, kSampleSize, r_lo, hist, c, t_lo,
-                        unused);
-    const uint32_t key_max = c.key_max;
-    const uint32_t range = key_max > t_lo ? key_max - t_lo : 0u;
-    const int bits = 32 - __clz(range);
-    const int bin_shift = bits > 9 ? bits - 9 : 0;
-
-    // Filter the staged chunk: keep keys >= t_lo, histogram them.
-    uint2 *lcand = reinterpret_cast<uint2 *>(ureg);
+    uint8_t *wrow = p.ws + kWsHeaderBytes + static_cast<size_t>(row) * p.plan.ws_row_bytes;
+    uint32_t *rhdr = reinterpret_cast<uint32_t *>(wrow);  // ticket, count, flags, t_lo, shift
+    uint32_t *ghist = reinterpret_cast<uint32_t *>(wrow + kRowHeaderBytes);
+    uint2 *gcand = reinterpret_cast<uint2 *>(wrow + kRowCounterBytes);
     for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
-    if (threadIdx.x == 0) c.cand_count = 0;
+    // the guess kernel's results: wait for it (programmatic dependent launch)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint32_t t_lo = __ldcg(&rhdr[3]);
+    const int bin_shift = static_cast<int>(__ldcg(&rhdr[4]));
+    GBTOPK_TRACE_POINT(2, 0);
     __syncthreads();
     const bool staged_ok = wait_stage(p, c, body);
-    if (staged_ok) {
-        constexpr int EPV = 16 / Elem<DT>::kBytes;
-        const int64_t nvec = ((off + len) * Elem<DT>::kBytes + 15) / 16;
-        const uint4 *svec = reinterpret_cast<const uint4 *>(stage);
-        for (int64_t vb = 0; vb < nvec; vb += blockDim.x) {
-            const int64_t v = vb + threadIdx.x;
-            uint4 w = make_uint4(0, 0, 0, 0);
-            if (v < nvec) w = svec[v];
-            const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int q = 0; q < EPV; ++q) {
-                const uint32_t raw = (Elem<DT>::kBytes == 4)
-                                         ? words[q]
-                                         : ((words[q >> 1] >> (16 * (q & 1))) & 0xFFFFu);
-                const int64_t el = v * EPV + q - off;
-                const uint32_t key = Elem<DT>::key(raw);
-                const bool pred = v < nvec && el >= 0 && el < len && key >= t_lo;
-                if (pred) {
-                    uint32_t bin = (key - t_lo) >> bin_shift;
-                    bin = bin < static_cast<uint32_t>(kBins - 1) ? bin : static_cast<uint32_t>(kBins - 1);
-                    atomicAdd(&hist[bin], 1u);
-                }
-                const uint32_t slot = warp_claim(&c.cand_count, pred);
-                if (pred && slot < static_cast<uint32_t>(kLocalCap))
-                    lcand[slot] = make_uint2(raw, static_cast<uint32_t>(c0 + el));
-            }
-        }
-    }
-    __syncthreads();
-
-    // Publish candidates and histogram to the row's workspace.
-    uint8_t *wrow = p.ws + kWsHeaderBytes + static_cast<size_t>(row) * p.plan.ws_row_bytes;
-    uint32_t *rhdr = reinterpret_cast<uint32_t *>(wrow);  // ticket, count, flags
-    uint32_t *ghist = reinterpret_cast<uint32_t *>(wrow + kRowHeaderBytes);
-    uint2 *gcand = reinterpret_cast<uint2 *>(wrow + kRowHeaderBytes + 4 * kBins);
+    GBTOPK_TRACE_POINT(3, 0);
     const uint32_t gcap = static_cast<uint32_t>(p.plan.gcap);
-    const uint32_t lc = c.cand_count;
-    if (threadIdx.x == 0) {
-        const uint32_t gb = staged_ok ? atomicAdd(&rhdr[1], lc) : 0u;
-        c.bcast[0] = gb;
-        if (!staged_ok || lc > static_cast<uint32_t>(kLocalCap) || gb + lc > gcap)
-            atomicOr(&rhdr[2], kRowOverflow);
-    }
-    __syncthreads();
+    uint32_t lc = 0;
     if (staged_ok) {
-        const uint32_t gb = c.bcast[0];
-        const uint32_t m = lc < static_cast<uint32_t>(kLocalCap) ? lc : kLocalCap;
-        for (uint32_t j = threadIdx.x; j < m; j += blockDim.x)
-            if (gb + j < gcap) gcand[gb + j] = lcand[j];
+        lc = filter_chunk<DT>(
+            stage, off, len, c0, t_lo, bin_shift, hist, c,
+            [&](uint32_t total) {
+                const uint32_t gb = atomicAdd(&rhdr[1], total);
+                if (gb + total > gcap) atomicOr(&rhdr[2], kRowOverflow);
+                return gb;
+            },
+            [&](uint32_t slot, uint32_t raw, uint32_t col) {
+                if (slot < gcap) gcand[slot] = make_uint2(raw, col);
+            });
         for (int b = threadIdx.x; b < kBins; b += blockDim.x)
             if (hist[b]) atomicAdd(&ghist[b], hist[b]);
+    } else if (threadIdx.x == 0) {
+        atomicOr(&rhdr[2], kRowOverflow);
     }
+    GBTOPK_TRACE_POINT(4, 0);
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -671,8 +943,11 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
         c.bcast[1] = (ticket == static_cast<uint32_t>(nch - 1)) ? 1u : 0u;
     }
     __syncthreads();
+    GBTOPK_TRACE_POINT(5, 0);
     if (c.bcast[1] == 0u) {
         drain_stage(c, body, staged_ok);
+        GBTOPK_TRACE_POINT(6, 0);
+        GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | 3u);
         return;
     }
 
@@ -681,89 +956,24 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
     const uint32_t total = __ldcg(&rhdr[1]);
     const uint32_t flags = __ldcg(&rhdr[2]);
     bool fallback = flags != 0u || total < static_cast<uint32_t>(k);
-    uint2 *blist = reinterpret_cast<uint2 *>(stage);
-    const uint32_t bcap = static_cast<uint32_t>((p.plan.smem - p.plan.off_stage) / sizeof(uint2));
-    uint32_t bstar = 0, above = 0, bsize = 0;
     if (!fallback) {
         for (int b = threadIdx.x; b < kBins; b += blockDim.x) hist[b] = __ldcg(&ghist[b]);
         __syncthreads();
-        // thread t owns bins kBins-1-4t .. kBins-4-4t (top first)
-        constexpr int BPT = kBins / kThreads;
-        uint32_t local[BPT], s = 0;
-#pragma unroll
-        for (int j = 0; j < BPT; ++j) {
-            local[j] = hist[kBins - 1 - BPT * threadIdx.x - j];
-            s += local[j];
-        }
-        uint32_t tot;
-        const uint32_t excl = block_excl_scan(s, c, tot);
-        if (excl < static_cast<uint32_t>(k) && static_cast<uint32_t>(k) <= excl + s) {
-            uint32_t acc = excl;
-#pragma unroll
-            for (int j = 0; j < BPT; ++j) {
-                if (acc + local[j] >= static_cast<uint32_t>(k)) {
-                    c.bcast[2] = kBins - 1 - BPT * threadIdx.x - j;
-                    c.bcast[3] = acc;
-                    c.bcast[4] = local[j];
-                    break;
-                }
-                acc += local[j];
-            }
-        }
-        __syncthreads();
-        bstar = c.bcast[2];
-        above = c.bcast[3];
-        bsize = c.bcast[4];
-        fallback = bsize > bcap;
+        fallback = !select_from_candidates<DT>(GlobalPairSrc<DT>{gcand}, total, hist, t_lo, bin_shift,
+                                               k, det, sel, reinterpret_cast<uint2 *>(stage),
+                                               stage_pairs, c);
     }
-    if (!fallback) {
-        if (threadIdx.x == 0) {
-            c.sel_count = 0;
-            c.b_count = 0;
-        }
-        __syncthreads();
-        for (uint32_t jb = 0; jb < total; jb += blockDim.x) {
-            const uint32_t j = jb + threadIdx.x;
-            uint2 v = make_uint2(0, 0);
-            const bool valid = j < total;
-            if (valid) v = __ldcg(gcand + j);
-            const uint32_t key = Elem<DT>::key(v.x);
-            uint32_t bin = (key - t_lo) >> bin_shift;
-            bin = bin < static_cast<uint32_t>(kBins - 1) ? bin : static_cast<uint32_t>(kBins - 1);
-            const bool hi = valid && bin > bstar;
-            const bool eq = valid && bin == bstar;
-            const uint32_t slot = warp_claim(&c.sel_count, hi);
-            if (hi) sel[slot] = v;
-            const uint32_t bslot = warp_claim(&c.b_count, eq);
-            if (eq) blist[bslot] = v;
-        }
-        __syncthreads();
-        const uint32_t need = static_cast<uint32_t>(k) - above;
-        const PairSrc<DT> bs{blist};
-        uint32_t t, gt;
-        block_select<KB, KB / 8>(ByKey<PairSrc<DT>>{bs}, bsize, need, hist, c, t, gt);
-        const uint32_t need_ties = need - gt;
-        uint32_t col_max = 0xFFFFFFFFu;
-        if (det) {
-            uint32_t kk, g2;
-            block_select<32, 4>(ByTieColumn<PairSrc<DT>>{bs, t}, bsize, need_ties, hist, c, kk, g2);
-            col_max = ~kk;
-        }
-        collect<DT>(bs, bsize, t, gt, need_ties, det, col_max, sel, above, c);
-    } else {
-        exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, det, sel, hist, c);
-    }
+    if (fallback) exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, det, sel, c.rhist, c);
 
-    // Leave the row's workspace zero-filled for the next call.
+    // Leave the row's counters and histogram zero-filled for the next call.
     for (int b = threadIdx.x; b < kBins; b += blockDim.x) ghist[b] = 0u;
-    if (threadIdx.x == 0) {
-        rhdr[0] = 0u;
-        rhdr[1] = 0u;
-        rhdr[2] = 0u;
-    }
+    if (threadIdx.x < kRowHeaderBytes / 4) rhdr[threadIdx.x] = 0u;
     if (det) sort_selection<DT>(sel, k);
     emit<DT>(p, row, sel, k);
     drain_stage(c, body, staged_ok);
+    GBTOPK_TRACE_POINT(6, 0);
+    GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | (fallback ? 5u : 4u) |
+                              (static_cast<unsigned long long>(total) << 40));
 }
 
 template <int DT>
@@ -775,11 +985,34 @@ cudaError_t launch_dt(const Params &p, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured = p.plan.smem;
     }
-    topk_kernel<DT><<<static_cast<unsigned>(p.plan.grid), p.plan.threads, p.plan.smem, stream>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.plan.grid));
+    cfg.blockDim = dim3(p.plan.threads);
+    cfg.dynamicSmemBytes = p.plan.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (p.plan.split) {
+        guess_kernel<DT><<<static_cast<unsigned>(p.num_rows), kThreads, 0, stream>>>(p);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, topk_kernel<DT>, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 }  // namespace
+
+#ifdef GBTOPK_TRACE
+extern "C" int gbtopk_trace_read(void *host, size_t bytes) {
+    if (bytes > sizeof(g_trace)) bytes = sizeof(g_trace);
+    return cudaMemcpyFromSymbol(host, g_trace, bytes) == cudaSuccess ? 0 : -5;
+}
+#endif
 
 cudaError_t launch_topk(int dtype, const Params &p, cudaStream_t stream) {
     switch (dtype) {
