@@ -80,13 +80,13 @@ extern "C" {
  *               descending, column ascending).  Short rows (n_r <= top_k)
  *               come in column order when 0.
  *  workspace    device scratch of at least gbtopk_workspace_bytes(...) bytes,
- *               256-byte aligned, zero-filled before its first use.  Its
- *               layout is the same for every geometry: a status word, then
- *               per row a block of counters and a histogram that every call
- *               leaves zero-filled again, followed by candidate scratch.  So
- *               one workspace, zeroed once, serves any sequence of calls on
- *               one stream.  Calls that may overlap in time (different
- *               streams, concurrent graph replays) need separate workspaces.
+ *               256-byte aligned.  Its first 4 bytes are a status word that
+ *               should start at zero (see gbtopk_device_status); everything
+ *               else is scratch that each call writes before reading, so the
+ *               contents need no initialisation and one workspace serves any
+ *               sequence of calls on one stream.  Calls that may overlap in
+ *               time (different streams, concurrent graph replays) need
+ *               separate workspaces.
  *  stream       cudaStream_t.
  *
  * Returns GBTOPK_OK / GBTOPK_HINT_DISCARDED, or a negative status (nothing
@@ -163,11 +163,12 @@ int gbtopk_device_status(void *workspace, uint32_t *flags, void *stream);
 
 /*
  * gbtopk_plan_query — the launch plan for a geometry, for inspection and
- * tests.  Fills out[0..9] = {chunk elements per block, chunks per row,
- * threads per block, dynamic shared memory bytes, split (0/1), candidate
- * capacity per split row, grid size, workspace bytes, workspace bytes per
- * split row, leading bytes of each row block kept zero between calls}.  Returns GBTOPK_OK or
- * GBTOPK_EINVAL / GBTOPK_EUNSUPPORTED.
+ * tests.  Fills out[0..9] = {columns per stream chunk, chunks of the widest
+ * split row (1 when no row is split), longest row finished by the one-block
+ * row kernel, row-kernel shared memory bytes, split (0/1), candidate entries
+ * reserved per split row, stream-kernel shared memory bytes, finalize-kernel
+ * shared memory bytes, workspace bytes, workspace bytes per row}.  Returns
+ * GBTOPK_OK or GBTOPK_EINVAL / GBTOPK_EUNSUPPORTED.
  */
 int gbtopk_plan_query(int64_t num_rows, int64_t width, int32_t top_k, int dtype,
                       int64_t *out);

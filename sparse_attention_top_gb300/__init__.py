@@ -108,8 +108,8 @@ def gbtopk_workspace_bytes(num_rows: int, width: int, top_k: int, dtype: torch.d
 def gbtopk_plan_query(num_rows: int, width: int, top_k: int, dtype: torch.dtype) -> dict:
     out = (ctypes.c_int64 * 10)()
     _check(load_library().gbtopk_plan_query(num_rows, width, top_k, _DTYPES[dtype], out))
-    keys = ["chunk", "chunks_per_row", "threads", "smem_bytes", "split", "candidate_capacity",
-            "grid", "workspace_bytes", "ws_row_bytes", "ws_row_counter_bytes"]
+    keys = ["chunk", "chunks_per_row", "direct_max", "row_smem", "split", "row_candidates",
+            "stream_smem", "final_smem", "workspace_bytes", "ws_row_bytes"]
     return dict(zip(keys, list(out)))
 
 
@@ -154,10 +154,10 @@ def gbtopk_page_table_transform(scores: torch.Tensor, lengths: torch.Tensor,
         workspace.numel() * workspace.element_size(), s))
 
 
-# One zero-filled workspace per (device, stream), grown on demand.  The
-# library keeps its counters zero between calls and its layout does not
-# depend on the geometry, so one workspace serves every call on a stream.
-# Create it (by one eager call) before capturing a CUDA graph on that stream.
+# One workspace per (device, stream), grown on demand.  Apart from its
+# status word the library writes every workspace byte before reading it, so
+# one workspace serves every call on a stream.  Create it (by one eager
+# call) before capturing a CUDA graph on that stream.
 _WS = {}
 
 

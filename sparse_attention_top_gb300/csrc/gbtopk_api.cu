@@ -27,48 +27,63 @@ bool overlaps(const void *a, size_t an, const void *b, size_t bn) {
 
 // The plan depends only on (num_rows, width, top_k, dtype): never on the
 // contents of seq_lens / lengths, so it is fixed at CUDA-graph capture.
+//
+// Rows of up to direct_max columns are finished by the row kernel alone
+// (one block per row, the row staged in shared memory).  When the width
+// allows longer rows, those are split into chunks of kChunkBytes and run
+// through three kernels: the row kernel (threshold guess), the persistent
+// stream kernel (filter every chunk) and the finalize kernel (exact select).
 int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *plan) {
     if (num_rows < 0 || width < 0 || top_k < 1 ||
         (dtype != GBTOPK_F32 && dtype != GBTOPK_BF16 && dtype != GBTOPK_F16))
         return GBTOPK_EINVAL;
     if (top_k > GBTOPK_MAX_TOP_K) return GBTOPK_EUNSUPPORTED;
-    if (width > INT32_MAX) return GBTOPK_EUNSUPPORTED;
+    if (width > INT32_MAX || num_rows > INT32_MAX) return GBTOPK_EUNSUPPORTED;
     const int es = elem_bytes(dtype);
-    const int64_t chunk_max = kChunkBytes / es;
+    const int64_t chunk = kChunkBytes / es;
     Plan pl{};
-    pl.threads = kThreads;
     int sel_cap = 32;
     while (sel_cap < top_k) sel_cap <<= 1;
     pl.sel_cap = sel_cap;
-    if (width <= chunk_max) {
-        pl.chunk = static_cast<int32_t>(align_up(static_cast<size_t>(width < 1 ? 1 : width), 32));
-        pl.chunks_per_row = 1;
-        pl.split = 0;
-        pl.gcap = 0;
-    } else {
-        pl.chunk = static_cast<int32_t>(chunk_max);
-        pl.chunks_per_row = static_cast<int32_t>((width + chunk_max - 1) / chunk_max);
-        pl.split = 1;
-        // Fixed per-row layout (independent of top_k, dtype and width) so one
-        // workspace serves every geometry: candidate scratch of one call can
-        // never land under another call's counters.
-        pl.gcap = gbtopk::kRowCandCap;
-    }
-    pl.grid = num_rows * pl.chunks_per_row;
-    if (pl.grid > INT32_MAX) return GBTOPK_EUNSUPPORTED;
-    // Shared memory: control block | histogram (kBins counters; also the
-    // row sample and, once the histogram is consumed, the selection buffer)
-    // | staged chunk (also candidate / boundary-bin scratch).
+    pl.chunk = static_cast<int32_t>(chunk);
+    // histogram (kBins counters) followed by the sample (kSampleSize keys)
+    const size_t big_hist = static_cast<size_t>(kBins) * 4 + static_cast<size_t>(kSampleSize) * 4;
     size_t hist = static_cast<size_t>(sel_cap) * 8;
-    if (pl.split || width > kExactMax) {
-        hist = hist > static_cast<size_t>(kBins) * 4 ? hist : static_cast<size_t>(kBins) * 4;
-        hist = hist > static_cast<size_t>(kSampleSize) * 4 ? hist : static_cast<size_t>(kSampleSize) * 4;
+    if (width <= 2 * chunk) {
+        pl.split = 0;
+        pl.direct_max = static_cast<int32_t>(width);
+        pl.chunks_per_row = 1;
+        hist = hist > big_hist ? hist : big_hist;
+    } else {
+        pl.split = 1;
+        pl.direct_max = static_cast<int32_t>(2 * chunk);
+        pl.chunks_per_row = static_cast<int32_t>((width + chunk - 1) / chunk);
+        if (pl.chunks_per_row > kFinalThreads) return GBTOPK_EUNSUPPORTED;
+        hist = hist > big_hist ? hist : big_hist;
+        pl.block_rows = num_rows < kMaxBlockRows ? num_rows : kMaxBlockRows;
+        pl.stream_smem = kCtrlBytes + align_up(static_cast<size_t>(kMaxBlockRows + 1) * 16, 128) +
+                         static_cast<size_t>(kStages) * kStageBytes;
+        pl.final_smem = kCtrlBytes + kFinalHistBytes +
+                        static_cast<size_t>(kFinalCandCap + kFinalBCap) * sizeof(uint2);
+        // candidate entries per row: the largest chunks x per-chunk capacity
+        // over the row lengths the width allows (capacity shrinks as n grows,
+        // so within a chunk count the shortest row is the worst case)
+        int64_t entries = 0;
+        for (int64_t j = 3; j <= pl.chunks_per_row; ++j) {
+            int64_t n_min = (j - 1) * chunk + 1;
+            if (n_min <= pl.direct_max) n_min = pl.direct_max + 1;
+            if (n_min > width) break;
+            const int64_t e = j * static_cast<int64_t>(chunk_seg_cap(n_min, top_k, pl.chunk));
+            entries = e > entries ? e : entries;
+        }
+        pl.row_seg_entries = entries;
+        const size_t seg_off = align_up(kRowInfoBytes + 4 * static_cast<size_t>(pl.chunks_per_row), 16);
+        pl.ws_row_bytes = align_up(seg_off + 8 * static_cast<size_t>(entries), 256);
     }
-    const size_t stage = align_up((static_cast<size_t>(pl.chunk) + 16 / es) * es, 16);
+    const size_t stage = align_up(static_cast<size_t>(pl.direct_max) * es, 16) + 32;
     pl.off_hist = kCtrlBytes;
-    pl.off_stage = align_up(pl.off_hist + hist, 16);
-    pl.smem = pl.off_stage + stage;
-    pl.ws_row_bytes = pl.split ? kRowBytes : 0;
+    pl.off_stage = align_up(pl.off_hist + hist, 128);
+    pl.row_smem = pl.off_stage + stage;
     pl.ws_bytes = kWsHeaderBytes + static_cast<size_t>(num_rows) * pl.ws_row_bytes;
     *plan = pl;
     return GBTOPK_OK;
@@ -217,14 +232,14 @@ int gbtopk_plan_query(int64_t num_rows, int64_t width, int32_t top_k, int dtype,
     if (rc != GBTOPK_OK) return rc;
     out[0] = plan.chunk;
     out[1] = plan.chunks_per_row;
-    out[2] = plan.threads;
-    out[3] = static_cast<int64_t>(plan.smem);
+    out[2] = plan.direct_max;
+    out[3] = static_cast<int64_t>(plan.row_smem);
     out[4] = plan.split;
-    out[5] = plan.gcap;
-    out[6] = plan.grid;
-    out[7] = static_cast<int64_t>(plan.ws_bytes);
-    out[8] = static_cast<int64_t>(plan.ws_row_bytes);
-    out[9] = static_cast<int64_t>(gbtopk::kRowCounterBytes);
+    out[5] = plan.row_seg_entries;
+    out[6] = static_cast<int64_t>(plan.stream_smem);
+    out[7] = static_cast<int64_t>(plan.final_smem);
+    out[8] = static_cast<int64_t>(plan.ws_bytes);
+    out[9] = static_cast<int64_t>(plan.ws_row_bytes);
     return GBTOPK_OK;
 }
 

@@ -2,6 +2,7 @@
 // device code (gbtopk_kernels.cu).  Not part of the public ABI.
 #pragma once
 
+#include <cmath>
 #include <cstddef>
 #include <cstdint>
 
@@ -9,42 +10,42 @@
 
 namespace gbtopk {
 
-constexpr int kThreads = 256;          // threads per block
+constexpr int kThreads = 256;          // threads per block (row and stream kernels)
+constexpr int kFinalThreads = 512;     // threads per block of the finalize kernel
 constexpr int kSampleGroups = 256;     // one group of 8 consecutive columns per thread
 constexpr int kSampleSize = kSampleGroups * 8;
 constexpr int kBinBits = 12;
 constexpr int kBins = 1 << kBinBits;   // candidate histogram bins
 constexpr int kRankMax = 256;          // boundary-bin size resolved by rank counting
-constexpr int kExactMax = 3072;        // rows up to this length: plain exact radix select
 constexpr size_t kCtrlBytes = 2048;    // per-block control block (counters, scan, digit histogram)
-constexpr int kChunkBytes = 32768;     // staged bytes per block for split rows
+constexpr int kChunkBytes = 32768;     // bytes per stream chunk (one bulk copy)
+constexpr int kStages = 3;             // bulk-copy ring depth of the stream kernel
+constexpr int kStageBytes = kChunkBytes + 32;  // a chunk plus its 16-byte alignment slack
+constexpr int kStreamThreads = 288;    // stream kernel: 1 producer warp + 8 consumer warps
+constexpr int kFinalHistBytes = 16384; // finalize histogram / selection buffer
+constexpr int kMaxBlockRows = 2048;    // rows per launch of the split pipeline
+constexpr int kFinalCandCap = 8192;    // candidates the finalize kernel keeps in shared memory
+constexpr int kFinalBCap = 4096;       // boundary-bin members the finalize kernel can hold
 constexpr size_t kWsHeaderBytes = 256; // device status word + padding
-constexpr int kRowHeaderBytes = 32;    // ticket, count, flags, t_lo, bin shift, pad
-constexpr int kRowCandCap = 16384;     // candidates per split row (8 x the largest top_k)
-// Per-row workspace of a split row: header + histogram (kept zero between
-// calls), then candidate scratch.
-constexpr size_t kRowCounterBytes = kRowHeaderBytes + 4 * kBins;
-constexpr size_t kRowBytes = (kRowCounterBytes + 8 * static_cast<size_t>(kRowCandCap) + 255) / 256 * 256;
+constexpr size_t kRowInfoBytes = 16;   // t_lo, bin shift (written by the row kernel)
 constexpr uint32_t kSpinLimit = 1u << 22;
 
-// Per-row flags in the split-row workspace.
-constexpr uint32_t kRowOverflow = 1u;  // a block lost candidates: recompute the row
 // Bits of the device status word.
 constexpr uint32_t kStatusWaitTimeout = 1u;
 
 struct Plan {
-    int32_t chunk;        // columns staged per block
-    int32_t chunks_per_row;
-    int32_t threads;
-    int32_t split;        // 1 when rows wider than `chunk` are cut across blocks
-    int32_t gcap;         // candidate capacity per split row
-    int32_t sel_cap;      // power of two >= top_k (selection / sort buffer)
-    int64_t grid;
-    size_t smem;          // dynamic shared memory per block
-    size_t ws_row_bytes;  // per-row workspace bytes (split plans)
-    size_t ws_bytes;      // total workspace bytes
-    // shared-memory layout (byte offsets)
-    size_t off_hist, off_stage;
+    int32_t chunk;           // elements per stream chunk
+    int32_t direct_max;      // rows up to this length are finished by the row kernel
+    int32_t chunks_per_row;  // chunks of the widest split row (0: no split rows possible)
+    int32_t split;           // 1 when some row can exceed direct_max
+    int32_t sel_cap;         // power of two >= top_k
+    int32_t stream_grid;     // persistent stream blocks
+    int64_t row_seg_entries; // candidate entries reserved per split row
+    size_t row_smem, stream_smem, final_smem;
+    size_t off_hist, off_stage;  // row kernel layout
+    size_t ws_row_bytes;     // per-row workspace bytes (split plans)
+    size_t ws_bytes;         // total workspace bytes
+    int64_t block_rows;      // rows per launch of the split pipeline
 };
 
 // Kernel arguments.  Row-length source: varlen mode when seq_lens != null,
@@ -62,19 +63,42 @@ struct Params {
     int32_t *out_idx;
     void *out_val;
     int32_t *out_raw;
-    const int32_t *page_table;   // null: no transform
+    const int32_t *page_table;  // null: no transform
     int64_t pt_cols, pt_row_stride;
     const int32_t *pt_row_starts;
     int32_t page_size;
     int32_t pt_start_is_row_start;
-    uint8_t *ws;
+    uint8_t *ws;   // status word at ws[0]; per-row blocks from kWsHeaderBytes
+    int64_t row0;  // first row of this launch (the split pipeline runs in row blocks)
+    int64_t rows;  // rows of this launch
     Plan plan;
 };
+
+// Guess rank: the sample rank whose key is taken as the threshold guess,
+// r = e + 6 sqrt(e) + 2 with e = m k / n the expected number of sample
+// elements at or above the k-th largest of the row.  Single precision
+// (IEEE-rounded on host and device alike; FP64 is slow on this GPU).
+__host__ __device__ inline uint32_t guess_rank(int64_t n, int32_t k) {
+    const float e = static_cast<float>(kSampleSize) * static_cast<float>(k) / static_cast<float>(n);
+    float r = ceilf(e + 6.0f * sqrtf(e) + 2.0f);
+    if (r > static_cast<float>(kSampleSize)) r = static_cast<float>(kSampleSize);
+    return static_cast<uint32_t>(r);
+}
+
+// Candidate capacity of one chunk of a split row with n valid columns (1.5x
+// the guessed fraction of the chunk plus 256, in multiples of 64); the same
+// arithmetic on host (workspace sizing) and device.
+__host__ __device__ inline int32_t chunk_seg_cap(int64_t n, int32_t k, int32_t chunk) {
+    const uint32_t r = guess_rank(n, k);
+    const int64_t cap = (3 * static_cast<int64_t>(r) * chunk) / (2 * kSampleSize) + 256;
+    const int64_t c = cap < chunk ? cap : chunk;
+    return static_cast<int32_t>((c + 63) / 64 * 64);
+}
 
 // Builds the launch plan; returns a gbtopk status.
 int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *plan);
 
-// Enqueues the selection kernel (device code lives in gbtopk_kernels.cu).
+// Enqueues the kernels of one call (device code lives in gbtopk_kernels.cu).
 cudaError_t launch_topk(int dtype, const Params &p, cudaStream_t stream);
 
 }  // namespace gbtopk

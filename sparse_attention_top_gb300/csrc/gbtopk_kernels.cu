@@ -40,14 +40,15 @@ namespace gbtopk {
 // Phase timestamps (%globaltimer, ns) of the first kTraceBlocks blocks, for
 // builds compiled with -DGBTOPK_TRACE (read back by gbtopk_trace_read).
 constexpr int kTraceBlocks = 1 << 16;
-__device__ unsigned long long g_trace[kTraceBlocks][8];
-#define GBTOPK_TRACE_POINT(slot, value)                                        \
-    do {                                                                       \
-        if (threadIdx.x == 0 && blockIdx.x < kTraceBlocks) {                   \
-            unsigned long long t_;                                             \
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));             \
-            g_trace[blockIdx.x][slot] = (slot) == 7 ? (value) : t_;            \
-        }                                                                      \
+__device__ unsigned long long g_trace[kTraceBlocks][16];
+// Each kernel declares kTraceBase: its blocks use g_trace[kTraceBase + block].
+#define GBTOPK_TRACE_POINT(slot, value)                                                      \
+    do {                                                                                     \
+        if (threadIdx.x == 0 && kTraceBase + blockIdx.x < kTraceBlocks) {                    \
+            unsigned long long t_;                                                           \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                           \
+            g_trace[kTraceBase + blockIdx.x][slot] = ((slot) == 7 || (slot) == 15) ? (value) : t_; \
+        }                                                                                    \
     } while (0)
 #else
 #define GBTOPK_TRACE_POINT(slot, value) \
@@ -110,6 +111,11 @@ struct Ctrl {
     uint32_t pad[3];
     uint32_t scan[72];
     uint32_t rhist[256];     // radix-select digit histogram
+    uint32_t key_min;
+    unsigned long long full[kStages];   // stream ring: stage filled (bulk copy landed)
+    unsigned long long empty[kStages];  // stream ring: stage read by every consumer warp
+    uint32_t scnt[2][kStages];          // stream ring: candidates of the stage's chunk
+    uint32_t sarr[2][kStages];          // stream ring: consumer warps done with the chunk
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
@@ -508,67 +514,47 @@ __device__ void emit(const Params &p, int64_t row, const uint2 *sel, int m) {
     }
 }
 
-// Stages elements [0, len) of `src` into shared memory: the 16-byte aligned
-// body by one bulk asynchronous copy, the unaligned head and tail by plain
-// loads.  Element e lands at stage[off + e].  Returns the body byte count
-// (0: nothing to wait for).  Thread 0 issues the copy.
+// ---------------------------------------------------------------- bulk staging
+
+// A span of elements staged by one bulk copy: the copy covers the 16-byte
+// aligned bytes [a0, a1) around the elements, so element e of the span lands
+// at stage[off + e].  The bytes outside the span (at most 15 on each side,
+// inside the same allocation) are copied but never used.
+struct Span {
+    const uint8_t *a0;
+    uint32_t bytes;
+    int32_t off;
+};
+
 template <int DT>
-__device__ uint32_t stage_row(const typename Elem<DT>::raw_t *src, int64_t len,
-                              typename Elem<DT>::raw_t *stage, unsigned long long *bar, int &off) {
+__device__ __forceinline__ Span span_of(const typename Elem<DT>::raw_t *src, int64_t len) {
     constexpr int es = Elem<DT>::kBytes;
-    const uint32_t mis = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u);
-    off = static_cast<int>(mis / es);
-    int64_t head = static_cast<int64_t>(((16u - mis) & 15u) / es);
-    if (head > len) head = len;
-    const uint32_t body_bytes = static_cast<uint32_t>(((len - head) * es) & ~static_cast<int64_t>(15));
-    const int64_t body_end = head + body_bytes / es;
-    if (threadIdx.x == 0 && body_bytes) bulk_load(stage + off + head, src + head, body_bytes, bar);
-    for (int64_t e = threadIdx.x; e < head; e += blockDim.x) stage[off + e] = __ldg(src + e);
-    for (int64_t e = body_end + threadIdx.x; e < len; e += blockDim.x) stage[off + e] = __ldg(src + e);
-    return body_bytes;
+    const uintptr_t b = reinterpret_cast<uintptr_t>(src);
+    const uintptr_t a0 = b & ~static_cast<uintptr_t>(15);
+    const uintptr_t a1 = (b + static_cast<uintptr_t>(len) * es + 15) & ~static_cast<uintptr_t>(15);
+    Span sp;
+    sp.a0 = reinterpret_cast<const uint8_t *>(a0);
+    sp.bytes = static_cast<uint32_t>(a1 - a0);
+    sp.off = static_cast<int32_t>((b - a0) / es);
+    return sp;
 }
 
-// Block-uniform wait for the staged body.  On timeout the status word is
-// flagged and the caller recomputes from global memory.
-__device__ bool wait_stage(const Params &p, Ctrl &c, uint32_t body_bytes) {
-    if (body_bytes == 0) return true;
+// Block-uniform bounded wait on a stage barrier.  On timeout the status
+// word is flagged and false is returned (the caller recomputes from global
+// memory).
+__device__ bool wait_bar(uint8_t *ws, Ctrl &c, unsigned long long *bar, uint32_t parity) {
     if (threadIdx.x == 0) {
-        const bool ok = mbar_wait(&c.bar, 0);
+        const bool ok = mbar_wait(bar, parity);
         c.bcast[7] = ok ? 1u : 0u;
-        if (!ok) atomicOr(reinterpret_cast<uint32_t *>(p.ws), kStatusWaitTimeout);
+        if (!ok) atomicOr(reinterpret_cast<uint32_t *>(ws), kStatusWaitTimeout);
     }
     __syncthreads();
     const bool ok = c.bcast[7] != 0;
-    if (ok) mbar_wait(&c.bar, 0);  // completes at once; acquire for every thread
-    __syncthreads();
+    if (ok) mbar_wait(bar, parity);  // completes at once; acquire for every thread
     return ok;
 }
 
-__device__ void drain_stage(Ctrl &c, uint32_t body_bytes, bool waited_ok) {
-    if (threadIdx.x == 0 && body_bytes && !waited_ok) mbar_wait(&c.bar, 0);
-}
-
-// ---------------------------------------------------------------- threshold guess
-
-// From m sample keys in shared memory, the guess t_lo: the r-th largest
-// sample key truncated to its top 16 bits, with r chosen so that the count
-// of row elements >= t_lo falls below k only with a tiny probability
-// (r = e + 6 sqrt(e) + 2, e = m k / n the expected sample count at or above
-// the k-th largest).  Also the histogram scale: keys t_lo .. key_max map
-// onto the lower half of kBins bins.
-template <int DT>
-__device__ void guess_threshold(const uint32_t *sample, int m, int64_t n, int k, uint32_t key_max,
-                                Ctrl &c, uint32_t &t_lo, int &bin_shift) {
-    constexpr int KB = Elem<DT>::kKeyBits;
-    const double e = static_cast<double>(m) * k / static_cast<double>(n);
-    uint32_t r = static_cast<uint32_t>(ceil(e + 6.0 * sqrt(e) + 2.0));
-    if (r > static_cast<uint32_t>(m)) r = static_cast<uint32_t>(m);
-    uint32_t unused;
-    block_select<KB, 2>(KeyArraySrc{sample}, RankByKey{}, m, r, c.rhist, c, t_lo, unused);
-    const uint32_t range = key_max > t_lo ? key_max - t_lo : 0u;
-    const int bits = 32 - __clz(range);
-    bin_shift = bits > kBinBits - 1 ? bits - (kBinBits - 1) : 0;
-}
+// ---------------------------------------------------------------- element tests
 
 // Element q of a 16-byte vector holding 4 (fp32) or 8 (16-bit) raw values,
 // without a dynamically indexed local array.
@@ -585,68 +571,159 @@ __device__ __forceinline__ uint32_t bin_of(uint32_t key, uint32_t t_lo, int bin_
     return b < static_cast<uint32_t>(kBins - 1) ? b : static_cast<uint32_t>(kBins - 1);
 }
 
-// Keeps the staged elements whose key is >= t_lo.  Each thread first loads
-// its vectors into registers and marks passing elements in a bit mask; one
-// block scan then gives every thread its output slot, so candidates are
-// written without per-element atomics.  `reserve(total)` (thread 0) returns
-// the first slot; `put(slot, raw, col)` stores one candidate.  The key of
-// each candidate is also counted in hist (kBins bins).  Returns the number
-// of candidates of the chunk (block-uniform).
-template <int DT, class Reserve, class Put>
-__device__ uint32_t filter_chunk(const typename Elem<DT>::raw_t *stage, int off, int64_t len,
-                                 int64_t col_base, uint32_t t_lo, int bin_shift, uint32_t *hist,
-                                 Ctrl &c, Reserve &&reserve, Put &&put) {
+__device__ __forceinline__ float float_of_key(uint32_t t) {
+    return __uint_as_float((t & 0x80000000u) ? (t & 0x7FFFFFFFu) : ~t);
+}
+
+// Threshold test of one raw element: key(raw) >= t_lo.  For fp32 it is one
+// float compare against the float whose key is t_lo (signed zeros compare
+// equal in IEEE arithmetic, so the two tests agree).
+template <int DT>
+struct PassTest {
+    uint32_t t_lo;
+    float tf;
+    __device__ __forceinline__ explicit PassTest(uint32_t t) : t_lo(t), tf(float_of_key(t)) {}
+    __device__ __forceinline__ bool operator()(uint32_t raw) const {
+        if (Elem<DT>::kBytes == 4) return __uint_as_float(raw) >= tf;
+        return Elem<DT>::key(raw) >= t_lo;
+    }
+};
+
+// Lanes of a staged 16-byte vector v that hold elements [0, len) of a span
+// whose element 0 sits at element position `off` of the stage.
+template <int EPV>
+__device__ __forceinline__ uint32_t valid_lanes(int v, int nvec, int off, int len) {
+    const int e0 = v * EPV - off;
+    const int lo = e0 < 0 ? -e0 : 0;
+    const int hi = (len - e0) < EPV ? (len - e0) : EPV;
+    return (v < nvec && hi > lo) ? (((1u << hi) - 1u) & ~((1u << lo) - 1u)) : 0u;
+}
+
+// ---------------------------------------------------------------- threshold guess
+
+// Block-wide suffix search over kBins counters: the bin b holding the r-th
+// largest item (S(b+1) < r <= S(b), S = count from the top).  Writes b to
+// c.bcast[2], the count above it to c.bcast[3] and its own count to
+// c.bcast[4].  Requires 1 <= r <= sum of counts.
+template <int NT>
+__device__ void find_bin_from_top(const uint32_t *hist, uint32_t r, Ctrl &c) {
+    constexpr int BPT = kBins / NT;
+    uint32_t local[BPT], s = 0;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) {
+        local[j] = hist[kBins - 1 - BPT * threadIdx.x - j];
+        s += local[j];
+    }
+    uint32_t tot;
+    const uint32_t excl = block_excl_scan(s, c, tot);
+    if (excl < r && r <= excl + s) {
+        uint32_t acc = excl;
+#pragma unroll
+        for (int j = 0; j < BPT; ++j) {
+            if (acc + local[j] >= r) {
+                c.bcast[2] = kBins - 1 - BPT * threadIdx.x - j;
+                c.bcast[3] = acc;
+                c.bcast[4] = local[j];
+                break;
+            }
+            acc += local[j];
+        }
+    }
+    __syncthreads();
+}
+
+// Conservative rank-r threshold of m keys in shared memory whose range is
+// [kmin, kmax]: one histogram round over kBins bins spanning the range
+// (fine bins, so the shared-memory increments rarely collide); returns the
+// lower key edge of the bin that holds the r-th largest key, so at least r
+// keys are >= the result.
+template <int NT>
+__device__ uint32_t adaptive_threshold(const uint32_t *keys, int m, uint32_t r, uint32_t kmin,
+                                       uint32_t kmax, uint32_t *hist, Ctrl &c) {
+    const int bits = 32 - __clz(kmax - kmin);
+    const int shift = bits > kBinBits ? bits - kBinBits : 0;
+#pragma unroll
+    for (int j = 0; j < kBins / NT; ++j) hist[threadIdx.x + j * NT] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < m; i += NT) atomicAdd(&hist[(keys[i] - kmin) >> shift], 1u);
+    __syncthreads();
+    find_bin_from_top<NT>(hist, r, c);
+    return kmin + (c.bcast[2] << shift);
+}
+
+// The guess from a sample of m keys (with their min and max) of a row of n
+// columns: t_lo such that, with high probability, at least k row elements
+// are >= t_lo (the sample rank r = e + 6 sqrt(e) + 2, e = m k / n); and the
+// histogram scale mapping keys t_lo .. key_max onto the lower half of kBins.
+template <int NT>
+__device__ void guess_from_sample(const uint32_t *sample, int m, int64_t n, int k, uint32_t kmin,
+                                  uint32_t kmax, uint32_t *hist, Ctrl &c, uint32_t &t_lo,
+                                  int &bin_shift) {
+    uint32_t r = guess_rank(n, k);
+    if (r > static_cast<uint32_t>(m)) r = static_cast<uint32_t>(m);
+    t_lo = adaptive_threshold<NT>(sample, m, r, kmin, kmax, hist, c);
+    const int bits = 32 - __clz(kmax - t_lo);
+    bin_shift = bits > kBinBits - 1 ? bits - (kBinBits - 1) : 0;
+}
+
+// Block-wide min and max of one key per thread into c.key_min / c.key_max
+// (which thread 0 must have reset to ~0u / 0 before a preceding barrier).
+__device__ __forceinline__ void block_minmax(uint32_t kmin, uint32_t kmax, Ctrl &c) {
+    kmin = __reduce_min_sync(0xffffffffu, kmin);
+    kmax = __reduce_max_sync(0xffffffffu, kmax);
+    if (lane_id() == 0) {
+        atomicMin(&c.key_min, kmin);
+        atomicMax(&c.key_max, kmax);
+    }
+    __syncthreads();
+}
+
+// ---------------------------------------------------------------- block filter
+
+// Keeps the staged elements [off, off + len) of `stage` whose key is >= t_lo.
+// Each thread loads its vectors (strided by the block size) into registers
+// and marks passing elements in bit masks; one block scan then gives each
+// thread its output slot, so candidates are written without per-element
+// atomics.  put(slot, raw, col) stores one candidate (col = col_base + e).
+// Returns the candidate count (block-uniform).  The staged bytes may be
+// overwritten by put() (every thread holds its vectors by then).
+template <int DT, int VPT, class Put>
+__device__ uint32_t filter_staged(const void *stage, int off, int len, int col_base, uint32_t t_lo,
+                                  Ctrl &c, Put &&put) {
     constexpr int es = Elem<DT>::kBytes;
     constexpr int EPV = 16 / es;
-    constexpr int VPT = (kChunkBytes + 16) / 16 / kThreads + 1;
-    const int64_t nvec = ((off + len) * es + 15) / 16;
-    const uint4 *svec = reinterpret_cast<const uint4 *>(stage);
+    const int nvec = ((off + len) * es + 15) >> 4;
+    const uint4 *svec = static_cast<const uint4 *>(stage);
     uint4 w[VPT];
-    uint32_t msk[VPT];
-    uint32_t cnt = 0;
-    const float tf = __uint_as_float((t_lo & 0x80000000u) ? (t_lo & 0x7FFFFFFFu) : ~t_lo);
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-        const int64_t v = threadIdx.x + static_cast<int64_t>(j) * kThreads;
+        const int v = threadIdx.x + j * static_cast<int>(blockDim.x);
         w[j] = v < nvec ? svec[v] : make_uint4(0, 0, 0, 0);
     }
+    const PassTest<DT> pass(t_lo);
+    uint32_t msk[VPT];
+    uint32_t cnt = 0;
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-        const int64_t v = threadIdx.x + static_cast<int64_t>(j) * kThreads;
-        // lanes of this vector that hold elements [0, len)
-        const int64_t e0 = v * EPV - off;
-        int lo = e0 < 0 ? static_cast<int>(-e0) : 0;
-        int hi = (len - e0) < EPV ? static_cast<int>(len - e0) : EPV;
-        uint32_t valid = 0;
-        if (v < nvec && hi > lo) valid = ((1u << hi) - 1u) & ~((1u << lo) - 1u);
+        const int v = threadIdx.x + j * static_cast<int>(blockDim.x);
         uint32_t m = 0;
 #pragma unroll
-        for (int q = 0; q < EPV; ++q) {
-            const uint32_t raw = vec_elem<es>(w[j], q);
-            const bool pass = es == 4 ? __uint_as_float(raw) >= tf : Elem<DT>::key(raw) >= t_lo;
-            m |= static_cast<uint32_t>(pass) << q;
-        }
-        msk[j] = m & valid;
+        for (int q = 0; q < EPV; ++q) m |= static_cast<uint32_t>(pass(vec_elem<es>(w[j], q))) << q;
+        msk[j] = m & valid_lanes<EPV>(v, nvec, off, len);
         cnt += __popc(msk[j]);
     }
     uint32_t total;
-    const uint32_t excl = block_excl_scan(cnt, c, total);
-    if (threadIdx.x == 0) c.bcast[0] = reserve(total);
-    __syncthreads();
-    uint32_t slot = c.bcast[0] + excl;
+    uint32_t slot = block_excl_scan(cnt, c, total);
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         uint32_t m = msk[j];
-        const int64_t v = threadIdx.x + static_cast<int64_t>(j) * kThreads;
+        const int v = threadIdx.x + j * static_cast<int>(blockDim.x);
         while (m) {
             const int q = __ffs(m) - 1;
             m &= m - 1;
-            const uint32_t raw = vec_elem<es>(w[j], q);
-            atomicAdd(&hist[bin_of(Elem<DT>::key(raw), t_lo, bin_shift)], 1u);
-            put(slot++, raw, static_cast<uint32_t>(col_base + v * EPV + q - off));
+            put(slot++, vec_elem<es>(w[j], q), static_cast<uint32_t>(col_base + v * EPV + q - off));
         }
     }
-    __syncthreads();
     return total;
 }
 
@@ -656,33 +733,12 @@ __device__ uint32_t filter_chunk(const typename Elem<DT>::raw_t *stage, int off,
 // b* (ranked by key, then by smaller column).  Writes sel[0..k).  Returns
 // false when bin b* holds more candidates than `bcap` (caller falls back).
 // `sel` may alias `hist` (the histogram is consumed first).
-template <int DT, class CandSrc>
-__device__ bool select_from_candidates(const CandSrc &cands, uint32_t total, uint32_t *hist,
+template <int DT, int NT, class CandSrc>
+__device__ bool select_from_candidates(const CandSrc &cands, uint32_t total, const uint32_t *hist,
                                        uint32_t t_lo, int bin_shift, int k, bool det, uint2 *sel,
                                        uint2 *blist, uint32_t bcap, Ctrl &c) {
-    constexpr int BPT = kBins / kThreads;
     constexpr int KB = Elem<DT>::kKeyBits;
-    uint32_t local[BPT], s = 0;
-#pragma unroll
-    for (int j = 0; j < BPT; ++j) {
-        local[j] = hist[kBins - 1 - BPT * threadIdx.x - j];
-        s += local[j];
-    }
-    uint32_t tot;
-    const uint32_t excl = block_excl_scan(s, c, tot);
-    if (excl < static_cast<uint32_t>(k) && static_cast<uint32_t>(k) <= excl + s) {
-        uint32_t acc = excl;
-#pragma unroll
-        for (int j = 0; j < BPT; ++j) {
-            if (acc + local[j] >= static_cast<uint32_t>(k)) {
-                c.bcast[2] = kBins - 1 - BPT * threadIdx.x - j;
-                c.bcast[3] = acc;
-                c.bcast[4] = local[j];
-                break;
-            }
-            acc += local[j];
-        }
-    }
+    find_bin_from_top<NT>(hist, static_cast<uint32_t>(k), c);
     if (threadIdx.x == 0) {
         c.sel_count = 0;
         c.b_count = 0;
@@ -732,111 +788,101 @@ __device__ bool select_from_candidates(const CandSrc &cands, uint32_t total, uin
     return true;
 }
 
-// Samples m keys of a row staged in shared memory (single elements at a
-// fixed stride) into `sample`, and their maximum into c.key_max.
-template <int DT>
-__device__ void sample_staged(const typename Elem<DT>::raw_t *row, int64_t n, int m, uint32_t *sample,
-                              Ctrl &c) {
-    if (threadIdx.x == 0) c.key_max = 0;
-    __syncthreads();
-    uint32_t kmax = 0;
-    for (int i = threadIdx.x; i < m; i += blockDim.x) {
-        const uint32_t key = Elem<DT>::key(row[static_cast<int64_t>(i) * n / m]);
-        sample[i] = key;
-        kmax = key > kmax ? key : kmax;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const uint32_t y = __shfl_xor_sync(0xffffffffu, kmax, o);
-        kmax = y > kmax ? y : kmax;
-    }
-    if (lane_id() == 0) atomicMax(&c.key_max, kmax);
-    __syncthreads();
+// ---------------------------------------------------------------- workspace layout
+
+__device__ __forceinline__ uint8_t *row_ws(const Params &p, int64_t row) {
+    return p.ws + kWsHeaderBytes + static_cast<size_t>(row) * p.plan.ws_row_bytes;
+}
+__device__ __forceinline__ uint32_t *row_info(const Params &p, int64_t row) {
+    return reinterpret_cast<uint32_t *>(row_ws(p, row));
+}
+__device__ __forceinline__ uint32_t *row_counts(const Params &p, int64_t row) {
+    return reinterpret_cast<uint32_t *>(row_ws(p, row) + kRowInfoBytes);
+}
+__device__ __forceinline__ uint2 *row_segs(const Params &p, int64_t row) {
+    const size_t off = (kRowInfoBytes + 4 * static_cast<size_t>(p.plan.chunks_per_row) + 15) / 16 * 16;
+    return reinterpret_cast<uint2 *>(row_ws(p, row) + off);
+}
+
+__device__ __forceinline__ int64_t split_chunks(const Params &p, int64_t n) {
+    return n > p.plan.direct_max ? (n + p.plan.chunk - 1) / p.plan.chunk : 0;
 }
 
 // ---------------------------------------------------------------- kernels
 
-// Guess kernel: one block per split row computes the row's threshold guess
-// from a strided sample (256 groups of 8 consecutive columns), anchored at
-// the hint's argmax column when a hint is given, and stores it in the row's
-// workspace header.  It lets the main kernel launch at once (programmatic
-// dependent launch), so the main kernel's bulk copies overlap this work.
-template <int DT>
-__global__ void __launch_bounds__(kThreads) guess_kernel(const __grid_constant__ Params p) {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    __shared__ Ctrl c;
-    __shared__ uint32_t sample[kSampleSize];
-    const int64_t row = blockIdx.x;
-    int64_t n, col0;
-    row_window(p, row, n, col0);
-    if (n <= p.k || n <= p.plan.chunk) return;
-    const typename Elem<DT>::raw_t *xrow =
-        static_cast<const typename Elem<DT>::raw_t *>(p.x) + row * p.row_stride + col0;
-    if (threadIdx.x == 0) c.key_max = 0;
-    const int64_t pos = static_cast<int64_t>(threadIdx.x) * (n - 8) / (kSampleGroups - 1);
-    uint32_t kmax = 0;
-    uint32_t raw[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) raw[j] = ldg_raw(xrow + pos + j);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint32_t key = Elem<DT>::key(raw[j]);
-        sample[threadIdx.x * 8 + j] = key;
-        kmax = key > kmax ? key : kmax;
-    }
-    if (threadIdx.x == 0 && p.pre_idx) {  // hint anchor: previous argmax
-        const int32_t a = __ldg(p.pre_idx + (row / p.next_n) * p.k);
-        if (static_cast<uint64_t>(static_cast<uint32_t>(a)) < static_cast<uint64_t>(n)) {
-            const uint32_t key = Elem<DT>::key(ldg_raw(xrow + a));
-            kmax = key > kmax ? key : kmax;
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const uint32_t y = __shfl_xor_sync(0xffffffffu, kmax, o);
-        kmax = y > kmax ? y : kmax;
-    }
-    __syncthreads();
-    if (lane_id() == 0) atomicMax(&c.key_max, kmax);
-    __syncthreads();
-    uint32_t t_lo;
-    int bin_shift;
-    guess_threshold<DT>(sample, kSampleSize, n, p.k, c.key_max, c, t_lo, bin_shift);
-    if (threadIdx.x == 0) {
-        uint32_t *rhdr = reinterpret_cast<uint32_t *>(p.ws + kWsHeaderBytes +
-                                                      static_cast<size_t>(row) * p.plan.ws_row_bytes);
-        rhdr[3] = t_lo;
-        rhdr[4] = static_cast<uint32_t>(bin_shift);
-    }
-}
-
-// Main kernel: block b handles chunk b % C of row b / C.
-template <int DT>
-__global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ Params p) {
+// Row kernel: one block per row.  Empty and short rows (n <= k) and rows up
+// to direct_max columns are finished here (the row is staged in shared
+// memory by one bulk copy).  For longer rows it computes the threshold guess
+// from a strided sample (256 groups of 8 consecutive columns) and stores it
+// in the row's workspace for the stream and finalize kernels.  It releases
+// the dependent stream kernel (programmatic dependent launch) once its own
+// global loads are in, so the stream's bulk copies do not queue ahead of them.
+template <int DT, int VPT>
+__global__ void __launch_bounds__(kThreads) row_kernel(const __grid_constant__ Params p) {
     using raw_t = typename Elem<DT>::raw_t;
     extern __shared__ __align__(128) uint8_t smem[];
     Ctrl &c = *reinterpret_cast<Ctrl *>(smem);
     uint32_t *hist = reinterpret_cast<uint32_t *>(smem + p.plan.off_hist);
     uint2 *sel = reinterpret_cast<uint2 *>(smem + p.plan.off_hist);  // aliases hist
-    raw_t *stage = reinterpret_cast<raw_t *>(smem + p.plan.off_stage);
-    const uint32_t stage_pairs = static_cast<uint32_t>((p.plan.smem - p.plan.off_stage) / sizeof(uint2));
-
-    const int cpr = p.plan.chunks_per_row;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) / cpr;
-    const int chunk = static_cast<int>(blockIdx.x % cpr);
+    uint32_t *sample = reinterpret_cast<uint32_t *>(smem + p.plan.off_hist + kBins * 4);
+    uint8_t *stage = smem + p.plan.off_stage;
+    const uint32_t stage_pairs = static_cast<uint32_t>((p.plan.row_smem - p.plan.off_stage) / sizeof(uint2));
+    const int64_t row = p.row0 + blockIdx.x;
     const int k = p.k;
     const bool det = p.deterministic != 0;
+    constexpr int kTraceBase = 0;
+    (void)kTraceBase;
 
     GBTOPK_TRACE_POINT(0, 0);
     int64_t n, col0;
     row_window(p, row, n, col0);
-    GBTOPK_TRACE_POINT(1, 0);
     const raw_t *xrow = static_cast<const raw_t *>(p.x) + row * p.row_stride + col0;
+    if (threadIdx.x == 0) {
+        c.key_min = 0xFFFFFFFFu;
+        c.key_max = 0;
+    }
+
+    if (n > p.plan.direct_max) {
+        // ---- split row: threshold guess from a strided sample
+        const int64_t pos = static_cast<int64_t>(threadIdx.x) * (n - 8) / (kSampleGroups - 1);
+        uint32_t raw[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) raw[j] = ldg_raw(xrow + pos + j);
+        uint32_t kmin = 0xFFFFFFFFu, kmax = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t key = Elem<DT>::key(raw[j]);
+            sample[threadIdx.x * 8 + j] = key;
+            kmin = key < kmin ? key : kmin;
+            kmax = key > kmax ? key : kmax;
+        }
+        __syncthreads();
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        if (threadIdx.x == 0 && p.pre_idx) {  // hint anchor: previous argmax column
+            const int32_t a = __ldg(p.pre_idx + (row / p.next_n) * k);
+            if (static_cast<uint64_t>(static_cast<uint32_t>(a)) < static_cast<uint64_t>(n)) {
+                const uint32_t key = Elem<DT>::key(ldg_raw(xrow + a));
+                kmax = key > kmax ? key : kmax;
+            }
+        }
+        block_minmax(kmin, kmax, c);
+        uint32_t t_lo;
+        int bin_shift;
+        guess_from_sample<kThreads>(sample, kSampleSize, n, k, c.key_min, c.key_max, hist, c, t_lo,
+                                    bin_shift);
+        if (threadIdx.x == 0) {
+            uint32_t *info = row_info(p, row);
+            info[0] = t_lo;
+            info[1] = static_cast<uint32_t>(bin_shift);
+        }
+        GBTOPK_TRACE_POINT(6, 0);
+        GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | 3u);
+        return;
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- short and empty rows: every valid column, then -1
     if (n <= k) {
-        GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | (chunk ? 0u : 1u));
-        if (chunk != 0) return;
         const bool need_raw = det || p.out_val != nullptr;
         for (int j = threadIdx.x; j < n; j += blockDim.x)
             sel[j] = make_uint2(need_raw ? ldg_raw(xrow + j) : 0u, static_cast<uint32_t>(j));
@@ -844,164 +890,433 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const __grid_constant__ 
         if (det) sort_selection<DT>(sel, static_cast<int>(n));
         emit<DT>(p, row, sel, static_cast<int>(n));
         GBTOPK_TRACE_POINT(6, 0);
+        GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | 1u);
         return;
     }
 
-    const int64_t CH = p.plan.chunk;
-    const int64_t nch = (n + CH - 1) / CH;
-    if (chunk >= nch) {
-        GBTOPK_TRACE_POINT(7, static_cast<unsigned long long>(n) << 8);
-        return;
-    }
-
+    // ---- direct rows: stage the row, then guess, filter and select in shared memory
     if (threadIdx.x == 0) mbar_init(&c.bar);
     __syncthreads();
-
-    // ---- single-chunk rows: everything in shared memory
-    if (nch == 1) {
-        int off;
-        const uint32_t body = stage_row<DT>(xrow, n, stage, &c.bar, off);
-        __syncthreads();
-        const bool ok = wait_stage(p, c, body);
-        GBTOPK_TRACE_POINT(3, 0);
-        bool done = false;
-        if (ok && n > kExactMax) {
-            // sampled guess from the staged row, filter, exact select
-            uint32_t *sample = hist;  // dead before the histogram is built
-            sample_staged<DT>(stage + off, n, kSampleSize, sample, c);
-            uint32_t t_lo;
-            int bin_shift;
-            guess_threshold<DT>(sample, kSampleSize, n, k, c.key_max, c, t_lo, bin_shift);
-            for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
-            __syncthreads();
-            uint2 *lcand = reinterpret_cast<uint2 *>(stage);  // rows are in registers by then
-            const uint32_t total = filter_chunk<DT>(
-                stage, off, n, 0, t_lo, bin_shift, hist, c, [](uint32_t) { return 0u; },
-                [&](uint32_t slot, uint32_t raw, uint32_t col) {
-                    if (slot < stage_pairs) lcand[slot] = make_uint2(raw, col);
-                });
-            if (total >= static_cast<uint32_t>(k) && total <= stage_pairs) {
-                done = select_from_candidates<DT>(PairSrc<DT>{lcand}, total, hist, t_lo, bin_shift, k,
-                                                  det, sel, lcand + total, stage_pairs - total, c);
-            }
-            if (!done) exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, det, sel, c.rhist, c);
-            done = true;
-        }
-        if (!done) {
-            if (ok) exact_select<DT>(StageSrc<DT>{stage + off}, n, k, det, sel, c.rhist, c);
-            else exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, det, sel, c.rhist, c);
-        }
-        if (det) sort_selection<DT>(sel, k);
-        emit<DT>(p, row, sel, k);
-        drain_stage(c, body, ok);
-        GBTOPK_TRACE_POINT(6, 0);
-        GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | 2u);
-        return;
-    }
-
-    // ---- split rows
-    const int64_t c0 = static_cast<int64_t>(chunk) * CH;
-    const int64_t len = (n - c0) < CH ? (n - c0) : CH;
-    int off;
-    const uint32_t body = stage_row<DT>(xrow + c0, len, stage, &c.bar, off);
-    uint8_t *wrow = p.ws + kWsHeaderBytes + static_cast<size_t>(row) * p.plan.ws_row_bytes;
-    uint32_t *rhdr = reinterpret_cast<uint32_t *>(wrow);  // ticket, count, flags, t_lo, shift
-    uint32_t *ghist = reinterpret_cast<uint32_t *>(wrow + kRowHeaderBytes);
-    uint2 *gcand = reinterpret_cast<uint2 *>(wrow + kRowCounterBytes);
-    for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
-    // the guess kernel's results: wait for it (programmatic dependent launch)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const uint32_t t_lo = __ldcg(&rhdr[3]);
-    const int bin_shift = static_cast<int>(__ldcg(&rhdr[4]));
-    GBTOPK_TRACE_POINT(2, 0);
+    const Span sp = span_of<DT>(xrow, n);
+    if (threadIdx.x == 0) bulk_load(stage, sp.a0, sp.bytes, &c.bar);
+    const bool ok = wait_bar(p.ws, c, &c.bar, 0);
     __syncthreads();
-    const bool staged_ok = wait_stage(p, c, body);
     GBTOPK_TRACE_POINT(3, 0);
-    const uint32_t gcap = static_cast<uint32_t>(p.plan.gcap);
-    uint32_t lc = 0;
-    if (staged_ok) {
-        lc = filter_chunk<DT>(
-            stage, off, len, c0, t_lo, bin_shift, hist, c,
-            [&](uint32_t total) {
-                const uint32_t gb = atomicAdd(&rhdr[1], total);
-                if (gb + total > gcap) atomicOr(&rhdr[2], kRowOverflow);
-                return gb;
-            },
-            [&](uint32_t slot, uint32_t raw, uint32_t col) {
-                if (slot < gcap) gcand[slot] = make_uint2(raw, col);
-            });
-        for (int b = threadIdx.x; b < kBins; b += blockDim.x)
-            if (hist[b]) atomicAdd(&ghist[b], hist[b]);
-    } else if (threadIdx.x == 0) {
-        atomicOr(&rhdr[2], kRowOverflow);
-    }
-    GBTOPK_TRACE_POINT(4, 0);
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const uint32_t ticket = atomicAdd(&rhdr[0], 1u);
-        c.bcast[1] = (ticket == static_cast<uint32_t>(nch - 1)) ? 1u : 0u;
-    }
-    __syncthreads();
-    GBTOPK_TRACE_POINT(5, 0);
-    if (c.bcast[1] == 0u) {
-        drain_stage(c, body, staged_ok);
-        GBTOPK_TRACE_POINT(6, 0);
-        GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | 3u);
-        return;
-    }
-
-    // ---- last block of the row: exact k-th from histogram + candidates
-    __threadfence();
-    const uint32_t total = __ldcg(&rhdr[1]);
-    const uint32_t flags = __ldcg(&rhdr[2]);
-    bool fallback = flags != 0u || total < static_cast<uint32_t>(k);
-    if (!fallback) {
-        for (int b = threadIdx.x; b < kBins; b += blockDim.x) hist[b] = __ldcg(&ghist[b]);
+    const raw_t *srow = reinterpret_cast<const raw_t *>(stage) + sp.off;
+    bool done = false;
+    if (ok) {
+        const int m = n < kSampleSize ? static_cast<int>(n) : kSampleSize;
+        // n <= two chunks (< 2^16 columns): 16.16 fixed point positions are exact enough
+        const uint32_t stride = static_cast<uint32_t>((static_cast<uint64_t>(n) << 16) / m);
+        uint32_t kmin = 0xFFFFFFFFu, kmax = 0;
+        for (int i = threadIdx.x; i < m; i += blockDim.x) {
+            const uint32_t key = Elem<DT>::key(srow[(static_cast<uint64_t>(i) * stride) >> 16]);
+            sample[i] = key;
+            kmin = key < kmin ? key : kmin;
+            kmax = key > kmax ? key : kmax;
+        }
+        block_minmax(kmin, kmax, c);
+        uint32_t t_lo;
+        int bin_shift;
+        guess_from_sample<kThreads>(sample, m, n, k, c.key_min, c.key_max, hist, c, t_lo, bin_shift);
+#pragma unroll
+        for (int j = 0; j < kBins / kThreads; ++j) hist[threadIdx.x + j * kThreads] = 0;
         __syncthreads();
-        fallback = !select_from_candidates<DT>(GlobalPairSrc<DT>{gcand}, total, hist, t_lo, bin_shift,
-                                               k, det, sel, reinterpret_cast<uint2 *>(stage),
-                                               stage_pairs, c);
+        uint2 *lcand = reinterpret_cast<uint2 *>(stage);  // the row is in registers by then
+        const uint32_t total = filter_staged<DT, VPT>(
+            stage, sp.off, static_cast<int>(n), 0, t_lo, c, [&](uint32_t slot, uint32_t raw, uint32_t col) {
+                if (slot < stage_pairs) lcand[slot] = make_uint2(raw, col);
+                atomicAdd(&hist[bin_of(Elem<DT>::key(raw), t_lo, bin_shift)], 1u);
+            });
+        __syncthreads();
+        if (total >= static_cast<uint32_t>(k) && total <= stage_pairs)
+            done = select_from_candidates<DT, kThreads>(PairSrc<DT>{lcand}, total, hist, t_lo, bin_shift,
+                                                        k, det, sel, lcand + total, stage_pairs - total, c);
     }
-    if (fallback) exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, det, sel, c.rhist, c);
-
-    // Leave the row's counters and histogram zero-filled for the next call.
-    for (int b = threadIdx.x; b < kBins; b += blockDim.x) ghist[b] = 0u;
-    if (threadIdx.x < kRowHeaderBytes / 4) rhdr[threadIdx.x] = 0u;
+    if (!done) exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, det, sel, c.rhist, c);
     if (det) sort_selection<DT>(sel, k);
     emit<DT>(p, row, sel, k);
-    drain_stage(c, body, staged_ok);
+    if (!ok && threadIdx.x == 0) mbar_wait(&c.bar, 0);  // let the copy land before exit
+    GBTOPK_TRACE_POINT(6, 0);
+    GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | 2u);
+}
+
+// Stream kernel: persistent blocks (one per SM) walk the chunks of the split
+// rows, block b taking chunks b, b + G, b + 2G, ... of the dense row-major
+// chunk list.  Warp 0 is the producer: it maps chunks to rows and issues
+// their bulk copies into a ring of kStages shared-memory stages ("full"
+// barriers carry the byte counts).  The other warps are consumers: each
+// loads its slice of a stage into registers, releases the stage ("empty"
+// barrier), keeps the elements at or above the row's guess and appends them
+// to that chunk's fixed segment in the workspace (one shared atomic per warp
+// reserves the slots); the last warp to finish a chunk stores its count.
+// There is no block-wide barrier in the steady state.
+struct StageMeta {
+    int64_t c0;       // first column of the chunk
+    int32_t row;      // row index within this launch
+    int32_t len;
+    int32_t off;
+    int32_t seg_cap;
+    int32_t chunk;
+    int32_t pad;
+};
+
+struct RowFacts {
+    uint32_t prefix;   // dense number of the row's first chunk
+    int32_t n;         // valid columns
+    int32_t col0;      // column of local index 0
+    uint32_t t_lo;     // threshold guess (after the row kernel)
+};
+static_assert(sizeof(RowFacts) == 16, "row facts");
+
+__device__ __forceinline__ void mbar_init_count(unsigned long long *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(unsigned long long *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_constant__ Params p) {
+    using raw_t = typename Elem<DT>::raw_t;
+    constexpr int es = Elem<DT>::kBytes;
+    constexpr int EPV = 16 / es;
+    constexpr int NCW = kStreamThreads / 32 - 1;  // consumer warps
+    constexpr int VPL = (kChunkBytes + 16) / 16 / (NCW * 32) + 1;
+    extern __shared__ __align__(128) uint8_t smem[];
+    Ctrl &c = *reinterpret_cast<Ctrl *>(smem);
+    const int rows = static_cast<int>(p.rows);
+    RowFacts *rf = reinterpret_cast<RowFacts *>(smem + kCtrlBytes);  // rows + 1 entries
+    StageMeta *meta = reinterpret_cast<StageMeta *>(smem + kCtrlBytes - kStages * sizeof(StageMeta));
+    uint8_t *stages = smem + p.plan.stream_smem - static_cast<size_t>(kStages) * kStageBytes;
+    const int64_t CH = p.plan.chunk;
+    constexpr int kTraceBase = 32768;
+    (void)kTraceBase;
+    GBTOPK_TRACE_POINT(0, 0);
+
+    // dense numbering of the chunks of the split rows of this launch
+    constexpr int RPT = (kMaxBlockRows + kStreamThreads - 1) / kStreamThreads;
+    uint32_t nch_local[RPT], sum = 0;
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+        const int r = threadIdx.x * RPT + j;
+        uint32_t nc = 0;
+        if (r < rows) {
+            int64_t n, col0;
+            row_window(p, p.row0 + r, n, col0);
+            nc = static_cast<uint32_t>(split_chunks(p, n));
+            rf[r].n = static_cast<int32_t>(n);
+            rf[r].col0 = static_cast<int32_t>(col0);
+        }
+        nch_local[j] = nc;
+        sum += nc;
+    }
+    uint32_t total_items;
+    uint32_t acc = block_excl_scan(sum, c, total_items);
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+        const int r = threadIdx.x * RPT + j;
+        if (r <= rows) rf[r].prefix = acc;
+        acc += nch_local[j];
+    }
+    if (threadIdx.x == 0) {
+        rf[rows].prefix = total_items;
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init_count(&c.full[s], 1);
+            mbar_init_count(&c.empty[s], NCW);
+            c.scnt[0][s] = c.scnt[1][s] = 0;
+            c.sarr[0][s] = c.sarr[1][s] = 0;
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    const int64_t G = gridDim.x;
+    const int warp = threadIdx.x >> 5;
+    const uint32_t lane = lane_id();
+    if (warp == 0) {
+        // ---- producer
+        if (lane == 0) {
+            for (int64_t i = 0;; ++i) {
+                const int64_t item = blockIdx.x + i * G;
+                if (item >= total_items) break;
+                const int s = static_cast<int>(i % kStages);
+                if (i >= kStages) {
+                    const uint32_t par = static_cast<uint32_t>(((i / kStages) - 1) & 1);
+                    if (!mbar_wait(&c.empty[s], par)) {
+                        atomicOr(reinterpret_cast<uint32_t *>(p.ws), kStatusWaitTimeout);
+                        break;
+                    }
+                }
+                int lo = 0, hi = rows - 1;  // last row with prefix <= item
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (rf[mid].prefix <= item) lo = mid;
+                    else hi = mid - 1;
+                }
+                const RowFacts f = rf[lo];
+                const int64_t chunk = item - f.prefix;
+                const int64_t c0 = chunk * CH;
+                const int64_t len = (f.n - c0) < CH ? (f.n - c0) : CH;
+                const raw_t *src =
+                    static_cast<const raw_t *>(p.x) + (p.row0 + lo) * p.row_stride + f.col0 + c0;
+                const Span sp = span_of<DT>(src, len);
+                StageMeta &m = meta[s];
+                m.c0 = c0;
+                m.row = lo;
+                m.len = static_cast<int32_t>(len);
+                m.off = sp.off;
+                m.chunk = static_cast<int32_t>(chunk);
+                m.seg_cap = chunk_seg_cap(f.n, p.k, p.plan.chunk);
+                bulk_load(stages + static_cast<size_t>(s) * kStageBytes, sp.a0, sp.bytes, &c.full[s]);
+            }
+        }
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        GBTOPK_TRACE_POINT(6, 0);
+        return;
+    }
+
+    // ---- consumers: the row kernel's guesses (programmatic dependent launch)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int r = threadIdx.x - 32; r < rows; r += NCW * 32)
+        if (rf[r].n > p.plan.direct_max) rf[r].t_lo = __ldcg(row_info(p, p.row0 + r));
+    asm volatile("bar.sync 1, %0;" ::"r"(NCW * 32) : "memory");
+
+    const int cw = warp - 1;
+    for (int64_t i = 0;; ++i) {
+        const int64_t item = blockIdx.x + i * G;
+        if (item >= total_items) break;
+        const int s = static_cast<int>(i % kStages);
+        const uint32_t par = static_cast<uint32_t>((i / kStages) & 1);
+        const bool ok = mbar_wait(&c.full[s], par);
+        const StageMeta m = meta[s];
+        const int64_t grow = p.row0 + m.row;
+        uint32_t cnt = 0;
+        uint4 w[VPL];
+        uint32_t msk[VPL];
+        const int nvec = ((m.off + m.len) * es + 15) >> 4;
+        const uint4 *svec = reinterpret_cast<const uint4 *>(stages + static_cast<size_t>(s) * kStageBytes);
+        if (ok) {
+#pragma unroll
+            for (int j = 0; j < VPL; ++j) {
+                const int v = cw * 32 + static_cast<int>(lane) + j * NCW * 32;
+                w[j] = v < nvec ? svec[v] : make_uint4(0, 0, 0, 0);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.empty[s]);  // release: this warp's reads are done
+        if (!ok) {
+            if (lane == 0) {
+                atomicOr(reinterpret_cast<uint32_t *>(p.ws), kStatusWaitTimeout);
+                row_counts(p, grow)[m.chunk] = 0xFFFFFFFFu;  // finalize recomputes the row
+            }
+            continue;
+        }
+        const PassTest<DT> pass(rf[m.row].t_lo);
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+            const int v = cw * 32 + static_cast<int>(lane) + j * NCW * 32;
+            uint32_t bits = 0;
+#pragma unroll
+            for (int q = 0; q < EPV; ++q) bits |= static_cast<uint32_t>(pass(vec_elem<es>(w[j], q))) << q;
+            msk[j] = bits & valid_lanes<EPV>(v, nvec, m.off, m.len);
+            cnt += __popc(msk[j]);
+        }
+        // warp-level slot reservation
+        uint32_t incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= static_cast<uint32_t>(o)) incl += y;
+        }
+        const uint32_t wtotal = __shfl_sync(0xffffffffu, incl, 31);
+        uint32_t base = 0;
+        if (lane == 0 && wtotal) base = atomicAdd(&c.scnt[par][s], wtotal);
+        base = __shfl_sync(0xffffffffu, base, 0);
+        uint32_t slot = base + incl - cnt;
+        const uint32_t cap = static_cast<uint32_t>(m.seg_cap);
+        uint2 *seg = row_segs(p, grow) + static_cast<int64_t>(m.chunk) * m.seg_cap;
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+            uint32_t bits = msk[j];
+            const int v = cw * 32 + static_cast<int>(lane) + j * NCW * 32;
+            while (bits) {
+                const int q = __ffs(bits) - 1;
+                bits &= bits - 1;
+                if (slot < cap)
+                    seg[slot] = make_uint2(vec_elem<es>(w[j], q),
+                                           static_cast<uint32_t>(m.c0 + v * EPV + q - m.off));
+                ++slot;
+            }
+        }
+        if (lane == 0) {
+            __threadfence_block();
+            if (atomicAdd(&c.sarr[par][s], 1u) == NCW - 1) {  // last warp on this chunk
+                row_counts(p, grow)[m.chunk] = atomicExch(&c.scnt[par][s], 0u);
+                c.sarr[par][s] = 0;
+            }
+        }
+    }
+    GBTOPK_TRACE_POINT(6, 0);
+}
+
+// Finalize kernel: one block per split row gathers the row's chunk segments
+// into shared memory, histograms the candidates' keys, and selects the exact
+// top-k (falling back to an exact radix select over the row in global memory
+// when a segment overflowed or the guess was too high).
+template <int DT>
+__global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_constant__ Params p) {
+    using raw_t = typename Elem<DT>::raw_t;
+    extern __shared__ __align__(128) uint8_t smem[];
+    Ctrl &c = *reinterpret_cast<Ctrl *>(smem);
+    uint32_t *hist = reinterpret_cast<uint32_t *>(smem + kCtrlBytes);
+    uint2 *sel = reinterpret_cast<uint2 *>(smem + kCtrlBytes);  // aliases hist
+    uint2 *cand = reinterpret_cast<uint2 *>(smem + kCtrlBytes + kFinalHistBytes);
+    uint2 *blist = cand + kFinalCandCap;
+    const int64_t row = p.row0 + blockIdx.x;
+    const int k = p.k;
+    const bool det = p.deterministic != 0;
+    constexpr int kTraceBase = 40960;
+    (void)kTraceBase;
+    int64_t n, col0;
+    row_window(p, row, n, col0);
+    const int64_t nch = split_chunks(p, n);
+    if (nch == 0) return;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    GBTOPK_TRACE_POINT(0, 0);
+    const raw_t *xrow = static_cast<const raw_t *>(p.x) + row * p.row_stride + col0;
+    const uint32_t *info = row_info(p, row);
+    const uint32_t t_lo = __ldcg(info);
+    const int bin_shift = static_cast<int>(__ldcg(info + 1));
+    const uint32_t cap = static_cast<uint32_t>(chunk_seg_cap(n, k, p.plan.chunk));
+    const uint32_t *counts = row_counts(p, row);
+    const uint2 *segs = row_segs(p, row);
+
+    // chunk counts -> offsets (nch <= kFinalThreads, checked on the host)
+    const uint32_t my = threadIdx.x < nch ? __ldcg(counts + threadIdx.x) : 0u;
+    if (threadIdx.x == 0) c.bcast[5] = 0;
+    __syncthreads();
+    if (my > cap) atomicOr(&c.bcast[5], 1u);
+    uint32_t total;
+    const uint32_t base = block_excl_scan(my > cap ? 0u : my, c, total);
+    bool fallback = c.bcast[5] != 0 || total < static_cast<uint32_t>(k) ||
+                    total > static_cast<uint32_t>(kFinalCandCap);
+    if (!fallback) {
+        uint32_t *choff = hist;  // chunk offsets, consumed before the histogram is built
+        if (threadIdx.x < nch) choff[threadIdx.x] = base;
+        __syncthreads();
+        // gather: entry j of the concatenated segments is entry j - off[c]
+        // of chunk c's segment; eight loads in flight per thread
+        constexpr int GB = 8;
+        for (uint32_t base0 = 0; base0 < total; base0 += GB * kFinalThreads) {
+            uint2 v[GB];
+#pragma unroll
+            for (int u = 0; u < GB; ++u) {
+                const uint32_t j = base0 + u * kFinalThreads + threadIdx.x;
+                v[u] = make_uint2(0, 0);
+                if (j < total) {
+                    int lo = 0, hi = static_cast<int>(nch) - 1;  // last chunk with off <= j
+                    while (lo < hi) {
+                        const int mid = (lo + hi + 1) >> 1;
+                        if (choff[mid] <= j) lo = mid;
+                        else hi = mid - 1;
+                    }
+                    v[u] = __ldcg(segs + static_cast<int64_t>(lo) * cap + (j - choff[lo]));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < GB; ++u) {
+                const uint32_t j = base0 + u * kFinalThreads + threadIdx.x;
+                if (j < total) cand[j] = v[u];
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < kBins / kFinalThreads; ++j) hist[threadIdx.x + j * kFinalThreads] = 0;
+        __syncthreads();
+        for (uint32_t j = threadIdx.x; j < total; j += blockDim.x)
+            atomicAdd(&hist[bin_of(Elem<DT>::key(cand[j].x), t_lo, bin_shift)], 1u);
+        __syncthreads();
+        GBTOPK_TRACE_POINT(1, 0);
+        fallback = !select_from_candidates<DT, kFinalThreads>(PairSrc<DT>{cand}, total, hist, t_lo,
+                                                              bin_shift, k, det, sel, blist,
+                                                              kFinalBCap, c);
+    }
+    if (fallback) exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, det, sel, c.rhist, c);
+    GBTOPK_TRACE_POINT(2, 0);
+    if (det) sort_selection<DT>(sel, k);
+    emit<DT>(p, row, sel, k);
     GBTOPK_TRACE_POINT(6, 0);
     GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | (fallback ? 5u : 4u) |
                               (static_cast<unsigned long long>(total) << 40));
 }
 
-template <int DT>
-cudaError_t launch_dt(const Params &p, cudaStream_t stream) {
-    static size_t configured = 0;  // largest dynamic smem opted in so far
-    if (p.plan.smem > 48 * 1024 && p.plan.smem > configured) {
-        const cudaError_t e = cudaFuncSetAttribute(
-            topk_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.plan.smem));
+template <class K>
+cudaError_t set_smem(K kern, size_t bytes, size_t &configured) {
+    if (bytes > 48 * 1024 && bytes > configured) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
         if (e != cudaSuccess) return e;
-        configured = p.plan.smem;
+        configured = bytes;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.plan.grid));
-    cfg.blockDim = dim3(p.plan.threads);
-    cfg.dynamicSmemBytes = p.plan.smem;
-    cfg.stream = stream;
+    return cudaSuccess;
+}
+
+template <int DT, int VPT>
+cudaError_t launch_row(const Params &p, cudaStream_t stream) {
+    static size_t configured = 0;  // largest dynamic smem opted in so far
+    const cudaError_t e = set_smem(row_kernel<DT, VPT>, p.plan.row_smem, configured);
+    if (e != cudaSuccess) return e;
+    row_kernel<DT, VPT><<<static_cast<unsigned>(p.rows), kThreads, p.plan.row_smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+// Row-kernel variant by the vectors each thread holds for a direct row.
+template <int DT>
+cudaError_t launch_row_any(const Params &p, cudaStream_t stream) {
+    const int64_t vec = (static_cast<int64_t>(p.plan.direct_max) * Elem<DT>::kBytes + 16 + 15) / 16;
+    if (vec <= 3 * kThreads) return launch_row<DT, 3>(p, stream);
+    if (vec <= 9 * kThreads) return launch_row<DT, 9>(p, stream);
+    return launch_row<DT, 17>(p, stream);
+}
+
+template <int DT>
+cudaError_t launch_dt(const Params &p0, cudaStream_t stream) {
+    static size_t cfg_stream = 0, cfg_final = 0;  // largest opt-in so far
+    cudaError_t e;
+    if (!p0.plan.split) {
+        Params p = p0;
+        p.row0 = 0;
+        p.rows = p0.num_rows;
+        return launch_row_any<DT>(p, stream);
+    }
+    if ((e = set_smem(stream_kernel<DT>, p0.plan.stream_smem, cfg_stream)) != cudaSuccess) return e;
+    if ((e = set_smem(final_kernel<DT>, p0.plan.final_smem, cfg_final)) != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
-    if (p.plan.split) {
-        guess_kernel<DT><<<static_cast<unsigned>(p.num_rows), kThreads, 0, stream>>>(p);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    for (int64_t r0 = 0; r0 < p0.num_rows; r0 += p0.plan.block_rows) {
+        Params p = p0;
+        p.row0 = r0;
+        p.rows = (p0.num_rows - r0) < p0.plan.block_rows ? (p0.num_rows - r0) : p0.plan.block_rows;
+        if ((e = launch_row_any<DT>(p, stream)) != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(sms));
+        cfg.blockDim = dim3(kStreamThreads);
+        cfg.dynamicSmemBytes = p.plan.stream_smem;
+        cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&cfg, stream_kernel<DT>, p)) != cudaSuccess) return e;
+        cfg.gridDim = dim3(static_cast<unsigned>(p.rows));
+        cfg.blockDim = dim3(kFinalThreads);
+        cfg.dynamicSmemBytes = p.plan.final_smem;
+        if ((e = cudaLaunchKernelEx(&cfg, final_kernel<DT>, p)) != cudaSuccess) return e;
     }
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, topk_kernel<DT>, p);
-    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

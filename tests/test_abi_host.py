@@ -127,16 +127,19 @@ def test_plan_totality_and_consistency():
         dt = rnd.choice(dts)
         p = gb.gbtopk_plan_query(R, W, k, dt)
         es = 4 if dt == torch.float32 else 2
-        assert p["chunk"] * p["chunks_per_row"] >= W
-        assert p["grid"] == R * p["chunks_per_row"]
-        assert p["threads"] == 256
-        assert p["smem_bytes"] <= 227 * 1024
-        assert p["chunk"] * es <= 32768 + 32 * es
+        assert p["chunk"] * es == 32768
+        for key in ("row_smem", "stream_smem", "final_smem"):
+            assert p[key] <= 227 * 1024
+        # a stream block and a row block must fit on one SM together
+        assert p["row_smem"] + p["stream_smem"] + 2048 <= 228 * 1024
         if p["split"]:
-            assert p["chunks_per_row"] > 1 and p["candidate_capacity"] >= 4 * k
+            assert W > p["direct_max"] == 2 * p["chunk"]
+            assert p["chunk"] * p["chunks_per_row"] >= W
+            assert p["row_candidates"] >= k and p["ws_row_bytes"] >= 8 * p["row_candidates"]
         else:
-            assert p["chunks_per_row"] == 1
-        assert p["workspace_bytes"] == gb.gbtopk_workspace_bytes(R, W, k, dt) >= 256
+            assert p["direct_max"] == W and p["chunks_per_row"] == 1 and p["ws_row_bytes"] == 0
+        assert p["workspace_bytes"] == gb.gbtopk_workspace_bytes(R, W, k, dt) == \
+            256 + R * p["ws_row_bytes"]
     with pytest.raises(gb.GbtopkError):
         gb.gbtopk_plan_query(4, 100, 0, torch.float32)
     assert gb.gbtopk_workspace_bytes(4, 100, 0, torch.float32) == 0

@@ -233,7 +233,9 @@ def test_misaligned_hint_is_discarded(dev):
         assert any(issubclass(i.category, RuntimeWarning) for i in w)
 
 
-def test_output_canaries_and_workspace_restored(dev):
+def test_output_canaries_and_scratch_workspace(dev):
+    """Outputs are written exactly in place; the workspace is scratch (poisoned
+    here before every call, apart from the status word) and results repeat."""
     c = workloads.dsv32_decode(rows=5, width=70000, top_k=2048, hinted=True, seed=2090)
     R, k = 5, 2048
     x = c.logits.to(dev)
@@ -244,22 +246,21 @@ def test_output_canaries_and_workspace_restored(dev):
     out_v = vbuf[32:32 + R * k]
     ws = torch.zeros(gb.gbtopk_workspace_bytes(R, 70000, k, torch.float32), dtype=torch.uint8,
                      device=dev)
-    for _ in range(3):
+    n = _lengths(c)
+    ref = _oracle_rows(c.logits, n, k, range(R))
+    first = None
+    for it in range(3):
+        ws[256:].fill_(0xA7 + it)
         idx, val = gb.top_k_varlen(x, c.seq_lens.to(dev), k, pre_idx=c.pre_idx.to(dev),
                                    return_values=True, out_indices=out_i, out_values=out_v,
-                                   workspace=ws)
+                                   workspace=ws, deterministic=True)
         torch.cuda.synchronize(dev)
         assert bool((ibuf[:32] == canary).all()) and bool((ibuf[32 + R * k:] == canary).all())
         assert bool((vbuf[:32] == 1.25).all()) and bool((vbuf[32 + R * k:] == 1.25).all())
-        plan = gb.gbtopk_plan_query(R, 70000, k, torch.float32)
-        rb, cb = plan["ws_row_bytes"], plan["ws_row_counter_bytes"]
-        assert int(ws[:256].count_nonzero()) == 0
-        for r in range(R):
-            blk = ws[256 + r * rb: 256 + r * rb + cb]
-            assert int(blk.count_nonzero()) == 0, f"row {r}: counters not restored to zero"
-    n = _lengths(c)
-    ref = _oracle_rows(c.logits, n, k, range(R))
-    check_rows(c.logits, n, k, idx, ref, val)
+        check_rows(c.logits, n, k, idx, ref, val, deterministic=True)
+        if first is None:
+            first = idx.clone()
+        assert torch.equal(first, idx)
     assert gb.gbtopk_device_status(ws) == 0
 
 
