@@ -55,8 +55,9 @@ int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *p
         pl.chunks_per_row = 1;
         hist = hist > big_hist ? hist : big_hist;
     } else {
+        // every row longer than top_k runs through the split pipeline
         pl.split = 1;
-        pl.direct_max = static_cast<int32_t>(2 * chunk);
+        pl.direct_max = top_k;
         pl.chunks_per_row = static_cast<int32_t>((width + chunk - 1) / chunk);
         if (pl.chunks_per_row > kFinalThreads) return GBTOPK_EUNSUPPORTED;
         hist = hist > big_hist ? hist : big_hist;
@@ -69,10 +70,10 @@ int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *p
         // over the row lengths the width allows (capacity shrinks as n grows,
         // so within a chunk count the shortest row is the worst case)
         int64_t entries = 0;
-        for (int64_t j = 3; j <= pl.chunks_per_row; ++j) {
+        for (int64_t j = 1; j <= pl.chunks_per_row; ++j) {
             int64_t n_min = (j - 1) * chunk + 1;
             if (n_min <= pl.direct_max) n_min = pl.direct_max + 1;
-            if (n_min > width) break;
+            if (n_min > width || n_min > j * chunk) continue;
             const int64_t e = j * static_cast<int64_t>(chunk_seg_cap(n_min, top_k, pl.chunk));
             entries = e > entries ? e : entries;
         }
@@ -80,7 +81,8 @@ int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *p
         const size_t seg_off = align_up(kRowInfoBytes + 4 * static_cast<size_t>(pl.chunks_per_row), 16);
         pl.ws_row_bytes = align_up(seg_off + 8 * static_cast<size_t>(entries), 256);
     }
-    const size_t stage = align_up(static_cast<size_t>(pl.direct_max) * es, 16) + 32;
+    // the row kernel stages direct rows only in plans without a split pipeline
+    const size_t stage = pl.split ? 0 : align_up(static_cast<size_t>(pl.direct_max) * es, 16) + 32;
     pl.off_hist = kCtrlBytes;
     pl.off_stage = align_up(pl.off_hist + hist, 128);
     pl.row_smem = pl.off_stage + stage;

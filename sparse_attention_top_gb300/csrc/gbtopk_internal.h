@@ -19,9 +19,10 @@ constexpr int kBins = 1 << kBinBits;   // candidate histogram bins
 constexpr int kRankMax = 256;          // boundary-bin size resolved by rank counting
 constexpr size_t kCtrlBytes = 2048;    // per-block control block (counters, scan, digit histogram)
 constexpr int kChunkBytes = 32768;     // bytes per stream chunk (one bulk copy)
-constexpr int kStages = 3;             // bulk-copy ring depth of the stream kernel
+constexpr int kStages = 4;             // bulk-copy ring depth of the stream kernel
+constexpr int kGroupWarps = 8;         // consumer warps that share one chunk
 constexpr int kStageBytes = kChunkBytes + 32;  // a chunk plus its 16-byte alignment slack
-constexpr int kStreamThreads = 288;    // stream kernel: 1 producer warp + 8 consumer warps
+constexpr int kStreamThreads = 544;    // stream kernel: 1 producer warp + 16 consumer warps
 constexpr int kFinalHistBytes = 16384; // finalize histogram / selection buffer
 constexpr int kMaxBlockRows = 2048;    // rows per launch of the split pipeline
 constexpr int kFinalCandCap = 8192;    // candidates the finalize kernel keeps in shared memory

@@ -114,8 +114,9 @@ struct Ctrl {
     uint32_t key_min;
     unsigned long long full[kStages];   // stream ring: stage filled (bulk copy landed)
     unsigned long long empty[kStages];  // stream ring: stage read by every consumer warp
-    uint32_t scnt[2][kStages];          // stream ring: candidates of the stage's chunk
-    uint32_t sarr[2][kStages];          // stream ring: consumer warps done with the chunk
+    // stream ring: per stage and parity, candidates reserved (low word) and
+    // consumer warps done (high word) for the stage's chunk
+    unsigned long long scombo[2][kStages];
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
@@ -601,17 +602,17 @@ __device__ __forceinline__ uint32_t valid_lanes(int v, int nvec, int off, int le
 
 // ---------------------------------------------------------------- threshold guess
 
-// Block-wide suffix search over kBins counters: the bin b holding the r-th
+// Block-wide suffix search over NB counters: the bin b holding the r-th
 // largest item (S(b+1) < r <= S(b), S = count from the top).  Writes b to
 // c.bcast[2], the count above it to c.bcast[3] and its own count to
 // c.bcast[4].  Requires 1 <= r <= sum of counts.
-template <int NT>
+template <int NT, int NB = kBins>
 __device__ void find_bin_from_top(const uint32_t *hist, uint32_t r, Ctrl &c) {
-    constexpr int BPT = kBins / NT;
+    constexpr int BPT = NB / NT;
     uint32_t local[BPT], s = 0;
 #pragma unroll
     for (int j = 0; j < BPT; ++j) {
-        local[j] = hist[kBins - 1 - BPT * threadIdx.x - j];
+        local[j] = hist[NB - 1 - BPT * threadIdx.x - j];
         s += local[j];
     }
     uint32_t tot;
@@ -621,7 +622,7 @@ __device__ void find_bin_from_top(const uint32_t *hist, uint32_t r, Ctrl &c) {
 #pragma unroll
         for (int j = 0; j < BPT; ++j) {
             if (acc + local[j] >= r) {
-                c.bcast[2] = kBins - 1 - BPT * threadIdx.x - j;
+                c.bcast[2] = NB - 1 - BPT * threadIdx.x - j;
                 c.bcast[3] = acc;
                 c.bcast[4] = local[j];
                 break;
@@ -633,22 +634,40 @@ __device__ void find_bin_from_top(const uint32_t *hist, uint32_t r, Ctrl &c) {
 }
 
 // Conservative rank-r threshold of m keys in shared memory whose range is
-// [kmin, kmax]: one histogram round over kBins bins spanning the range
-// (fine bins, so the shared-memory increments rarely collide); returns the
-// lower key edge of the bin that holds the r-th largest key, so at least r
-// keys are >= the result.
-template <int NT>
+// [kmin, kmax]: a histogram round over NB bins spanning the range (fine
+// bins, so the shared-memory increments rarely collide) finds the bin that
+// holds the r-th largest key; a second round splits that bin into NB
+// sub-bins.  Returns the lower key edge of the sub-bin holding the r-th
+// largest key, so at least r keys are >= the result.
+template <int NT, int NB>
 __device__ uint32_t adaptive_threshold(const uint32_t *keys, int m, uint32_t r, uint32_t kmin,
                                        uint32_t kmax, uint32_t *hist, Ctrl &c) {
+    constexpr int NBITS = NB == 512 ? 9 : (NB == 1024 ? 10 : (NB == 2048 ? 11 : 12));
+    static_assert((1 << NBITS) == NB, "bin count");
     const int bits = 32 - __clz(kmax - kmin);
-    const int shift = bits > kBinBits ? bits - kBinBits : 0;
+    const int shift = bits > NBITS ? bits - NBITS : 0;
 #pragma unroll
-    for (int j = 0; j < kBins / NT; ++j) hist[threadIdx.x + j * NT] = 0;
+    for (int j = 0; j < NB / NT; ++j) hist[threadIdx.x + j * NT] = 0;
     __syncthreads();
     for (int i = threadIdx.x; i < m; i += NT) atomicAdd(&hist[(keys[i] - kmin) >> shift], 1u);
     __syncthreads();
-    find_bin_from_top<NT>(hist, r, c);
-    return kmin + (c.bcast[2] << shift);
+    find_bin_from_top<NT, NB>(hist, r, c);
+    const uint32_t b = c.bcast[2];
+    const uint32_t rem = r - c.bcast[3];
+    const uint32_t edge = kmin + (b << shift);
+    if (shift == 0 || c.bcast[4] == rem) return edge;  // exact key, or the whole bin is needed
+    const int shift2 = shift > NBITS ? shift - NBITS : 0;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < NB / NT; ++j) hist[threadIdx.x + j * NT] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < m; i += NT) {
+        const uint32_t d = keys[i] - kmin;
+        if ((d >> shift) == b) atomicAdd(&hist[(d - (b << shift)) >> shift2], 1u);
+    }
+    __syncthreads();
+    find_bin_from_top<NT, NB>(hist, rem, c);
+    return edge + (c.bcast[2] << shift2);
 }
 
 // The guess from a sample of m keys (with their min and max) of a row of n
@@ -661,7 +680,7 @@ __device__ void guess_from_sample(const uint32_t *sample, int m, int64_t n, int 
                                   int &bin_shift) {
     uint32_t r = guess_rank(n, k);
     if (r > static_cast<uint32_t>(m)) r = static_cast<uint32_t>(m);
-    t_lo = adaptive_threshold<NT>(sample, m, r, kmin, kmax, hist, c);
+    t_lo = adaptive_threshold<NT, 512>(sample, m, r, kmin, kmax, hist, c);
     const int bits = 32 - __clz(kmax - t_lo);
     bin_shift = bits > kBinBits - 1 ? bits - (kBinBits - 1) : 0;
 }
@@ -843,18 +862,31 @@ __global__ void __launch_bounds__(kThreads) row_kernel(const __grid_constant__ P
     }
 
     if (n > p.plan.direct_max) {
-        // ---- split row: threshold guess from a strided sample
-        const int64_t pos = static_cast<int64_t>(threadIdx.x) * (n - 8) / (kSampleGroups - 1);
-        uint32_t raw[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) raw[j] = ldg_raw(xrow + pos + j);
+        // ---- split row: threshold guess from a strided sample (the whole
+        // row when it has at most kSampleSize columns)
+        int m;
         uint32_t kmin = 0xFFFFFFFFu, kmax = 0;
+        if (n > kSampleSize) {
+            m = kSampleSize;
+            const int64_t pos = static_cast<int64_t>(threadIdx.x) * (n - 8) / (kSampleGroups - 1);
+            uint32_t raw[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint32_t key = Elem<DT>::key(raw[j]);
-            sample[threadIdx.x * 8 + j] = key;
-            kmin = key < kmin ? key : kmin;
-            kmax = key > kmax ? key : kmax;
+            for (int j = 0; j < 8; ++j) raw[j] = ldg_raw(xrow + pos + j);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t key = Elem<DT>::key(raw[j]);
+                sample[threadIdx.x * 8 + j] = key;
+                kmin = key < kmin ? key : kmin;
+                kmax = key > kmax ? key : kmax;
+            }
+        } else {
+            m = static_cast<int>(n);
+            for (int i = threadIdx.x; i < m; i += kThreads) {
+                const uint32_t key = Elem<DT>::key(ldg_raw(xrow + i));
+                sample[i] = key;
+                kmin = key < kmin ? key : kmin;
+                kmax = key > kmax ? key : kmax;
+            }
         }
         __syncthreads();
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -868,8 +900,7 @@ __global__ void __launch_bounds__(kThreads) row_kernel(const __grid_constant__ P
         block_minmax(kmin, kmax, c);
         uint32_t t_lo;
         int bin_shift;
-        guess_from_sample<kThreads>(sample, kSampleSize, n, k, c.key_min, c.key_max, hist, c, t_lo,
-                                    bin_shift);
+        guess_from_sample<kThreads>(sample, m, n, k, c.key_min, c.key_max, hist, c, t_lo, bin_shift);
         if (threadIdx.x == 0) {
             uint32_t *info = row_info(p, row);
             info[0] = t_lo;
@@ -895,6 +926,9 @@ __global__ void __launch_bounds__(kThreads) row_kernel(const __grid_constant__ P
     }
 
     // ---- direct rows: stage the row, then guess, filter and select in shared memory
+    if constexpr (VPT == 0) {
+        return;  // split plans: every row longer than top_k went to the guess above
+    } else {
     if (threadIdx.x == 0) mbar_init(&c.bar);
     __syncthreads();
     const Span sp = span_of<DT>(xrow, n);
@@ -939,6 +973,7 @@ __global__ void __launch_bounds__(kThreads) row_kernel(const __grid_constant__ P
     if (!ok && threadIdx.x == 0) mbar_wait(&c.bar, 0);  // let the copy land before exit
     GBTOPK_TRACE_POINT(6, 0);
     GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | 2u);
+    }
 }
 
 // Stream kernel: persistent blocks (one per SM) walk the chunks of the split
@@ -983,7 +1018,9 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
     constexpr int es = Elem<DT>::kBytes;
     constexpr int EPV = 16 / es;
     constexpr int NCW = kStreamThreads / 32 - 1;  // consumer warps
-    constexpr int VPL = (kChunkBytes + 16) / 16 / (NCW * 32) + 1;
+    constexpr int kGroups = NCW / kGroupWarps;      // consumer groups take alternate chunks
+    constexpr int VPL = (kChunkBytes + 16) / 16 / (kGroupWarps * 32) + 1;
+    static_assert(kStages % kGroups == 0, "each group cycles its own stages");
     extern __shared__ __align__(128) uint8_t smem[];
     Ctrl &c = *reinterpret_cast<Ctrl *>(smem);
     const int rows = static_cast<int>(p.rows);
@@ -1024,9 +1061,8 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
         rf[rows].prefix = total_items;
         for (int s = 0; s < kStages; ++s) {
             mbar_init_count(&c.full[s], 1);
-            mbar_init_count(&c.empty[s], NCW);
-            c.scnt[0][s] = c.scnt[1][s] = 0;
-            c.sarr[0][s] = c.sarr[1][s] = 0;
+            mbar_init_count(&c.empty[s], kGroupWarps);
+            c.scombo[0][s] = c.scombo[1][s] = 0;
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -1038,13 +1074,23 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
     if (warp == 0) {
         // ---- producer
         if (lane == 0) {
+#ifdef GBTOPK_TRACE
+            unsigned long long p_wait = 0;
+#endif
             for (int64_t i = 0;; ++i) {
                 const int64_t item = blockIdx.x + i * G;
                 if (item >= total_items) break;
                 const int s = static_cast<int>(i % kStages);
                 if (i >= kStages) {
                     const uint32_t par = static_cast<uint32_t>(((i / kStages) - 1) & 1);
+#ifdef GBTOPK_TRACE
+                    const unsigned long long pa = clock64();
+                    const bool got = mbar_wait(&c.empty[s], par);
+                    p_wait += clock64() - pa;
+                    if (!got) {
+#else
                     if (!mbar_wait(&c.empty[s], par)) {
+#endif
                         atomicOr(reinterpret_cast<uint32_t *>(p.ws), kStatusWaitTimeout);
                         break;
                     }
@@ -1071,6 +1117,9 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
                 m.seg_cap = chunk_seg_cap(f.n, p.k, p.plan.chunk);
                 bulk_load(stages + static_cast<size_t>(s) * kStageBytes, sp.a0, sp.bytes, &c.full[s]);
             }
+#ifdef GBTOPK_TRACE
+            if (kTraceBase + blockIdx.x < kTraceBlocks) g_trace[kTraceBase + blockIdx.x][12] = p_wait;
+#endif
         }
         asm volatile("griddepcontrol.wait;" ::: "memory");
         GBTOPK_TRACE_POINT(6, 0);
@@ -1084,23 +1133,35 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
     asm volatile("bar.sync 1, %0;" ::"r"(NCW * 32) : "memory");
 
     const int cw = warp - 1;
-    for (int64_t i = 0;; ++i) {
-        const int64_t item = blockIdx.x + i * G;
-        if (item >= total_items) break;
-        const int s = static_cast<int>(i % kStages);
+    const int grp = cw / kGroupWarps, gw = cw % kGroupWarps;
+    const int my_items = blockIdx.x < total_items
+                             ? static_cast<int>((total_items - blockIdx.x + G - 1) / G) : 0;
+#ifdef GBTOPK_TRACE
+    unsigned long long t_wait = 0, t_busy = 0, t_mark = clock64(), n_items = 0;
+#endif
+    for (int i = grp; i < my_items; i += kGroups) {
+        const int s = i % kStages;
         const uint32_t par = static_cast<uint32_t>((i / kStages) & 1);
+#ifdef GBTOPK_TRACE
+        unsigned long long t_a = clock64();
+        t_busy += t_a - t_mark;
+#endif
         const bool ok = mbar_wait(&c.full[s], par);
+#ifdef GBTOPK_TRACE
+        t_mark = clock64();
+        t_wait += t_mark - t_a;
+        ++n_items;
+#endif
         const StageMeta m = meta[s];
         const int64_t grow = p.row0 + m.row;
-        uint32_t cnt = 0;
-        uint4 w[VPL];
-        uint32_t msk[VPL];
         const int nvec = ((m.off + m.len) * es + 15) >> 4;
         const uint4 *svec = reinterpret_cast<const uint4 *>(stages + static_cast<size_t>(s) * kStageBytes);
+        const int vbase = gw * 32 + static_cast<int>(lane);
+        uint4 w[VPL];
         if (ok) {
 #pragma unroll
             for (int j = 0; j < VPL; ++j) {
-                const int v = cw * 32 + static_cast<int>(lane) + j * NCW * 32;
+                const int v = vbase + j * kGroupWarps * 32;
                 w[j] = v < nvec ? svec[v] : make_uint4(0, 0, 0, 0);
             }
         }
@@ -1114,16 +1175,19 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
             continue;
         }
         const PassTest<DT> pass(rf[m.row].t_lo);
+        uint32_t msk[VPL];
+        uint32_t cnt = 0;
 #pragma unroll
         for (int j = 0; j < VPL; ++j) {
-            const int v = cw * 32 + static_cast<int>(lane) + j * NCW * 32;
+            const int v = vbase + j * kGroupWarps * 32;
             uint32_t bits = 0;
 #pragma unroll
             for (int q = 0; q < EPV; ++q) bits |= static_cast<uint32_t>(pass(vec_elem<es>(w[j], q))) << q;
-            msk[j] = bits & valid_lanes<EPV>(v, nvec, m.off, m.len);
-            cnt += __popc(msk[j]);
+            if (v == 0 || v >= nvec - 1) bits &= valid_lanes<EPV>(v, nvec, m.off, m.len);
+            msk[j] = bits;
+            cnt += __popc(bits);
         }
-        // warp-level slot reservation
+        // warp-level slot reservation; the same atomic counts the warps done
         uint32_t incl = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -1131,34 +1195,40 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
             if (lane >= static_cast<uint32_t>(o)) incl += y;
         }
         const uint32_t wtotal = __shfl_sync(0xffffffffu, incl, 31);
-        uint32_t base = 0;
-        if (lane == 0 && wtotal) base = atomicAdd(&c.scnt[par][s], wtotal);
-        base = __shfl_sync(0xffffffffu, base, 0);
+        unsigned long long old = 0;
+        if (lane == 0) old = atomicAdd(&c.scombo[par][s], (1ull << 32) | wtotal);
+        const uint32_t base = __shfl_sync(0xffffffffu, static_cast<uint32_t>(old), 0);
+        if (lane == 0 && static_cast<uint32_t>(old >> 32) == kGroupWarps - 1) {  // last warp on the chunk
+            row_counts(p, grow)[m.chunk] = base + wtotal;
+            c.scombo[par][s] = 0;
+        }
         uint32_t slot = base + incl - cnt;
         const uint32_t cap = static_cast<uint32_t>(m.seg_cap);
         uint2 *seg = row_segs(p, grow) + static_cast<int64_t>(m.chunk) * m.seg_cap;
+        const int colbase = static_cast<int>(m.c0) - m.off;
 #pragma unroll
         for (int j = 0; j < VPL; ++j) {
             uint32_t bits = msk[j];
-            const int v = cw * 32 + static_cast<int>(lane) + j * NCW * 32;
+            const int vcol = colbase + (vbase + j * kGroupWarps * 32) * EPV;
             while (bits) {
                 const int q = __ffs(bits) - 1;
                 bits &= bits - 1;
-                if (slot < cap)
-                    seg[slot] = make_uint2(vec_elem<es>(w[j], q),
-                                           static_cast<uint32_t>(m.c0 + v * EPV + q - m.off));
+                if (slot < cap) seg[slot] = make_uint2(vec_elem<es>(w[j], q), static_cast<uint32_t>(vcol + q));
                 ++slot;
             }
         }
-        if (lane == 0) {
-            __threadfence_block();
-            if (atomicAdd(&c.sarr[par][s], 1u) == NCW - 1) {  // last warp on this chunk
-                row_counts(p, grow)[m.chunk] = atomicExch(&c.scnt[par][s], 0u);
-                c.sarr[par][s] = 0;
-            }
-        }
     }
-    GBTOPK_TRACE_POINT(6, 0);
+#ifdef GBTOPK_TRACE
+    t_busy += clock64() - t_mark;
+    if (threadIdx.x == 32 && kTraceBase + blockIdx.x < kTraceBlocks) {
+        g_trace[kTraceBase + blockIdx.x][8] = t_wait;
+        g_trace[kTraceBase + blockIdx.x][9] = t_busy;
+        g_trace[kTraceBase + blockIdx.x][10] = n_items;
+        unsigned long long t_;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));
+        g_trace[kTraceBase + blockIdx.x][11] = t_;
+    }
+#endif
 }
 
 // Finalize kernel: one block per split row gathers the row's chunk segments
@@ -1203,11 +1273,13 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
     bool fallback = c.bcast[5] != 0 || total < static_cast<uint32_t>(k) ||
                     total > static_cast<uint32_t>(kFinalCandCap);
     if (!fallback) {
-        uint32_t *choff = hist;  // chunk offsets, consumed before the histogram is built
+        uint32_t *choff = reinterpret_cast<uint32_t *>(blist);  // chunk offsets (blist is free yet)
         if (threadIdx.x < nch) choff[threadIdx.x] = base;
+#pragma unroll
+        for (int j = 0; j < kBins / kFinalThreads; ++j) hist[threadIdx.x + j * kFinalThreads] = 0;
         __syncthreads();
-        // gather: entry j of the concatenated segments is entry j - off[c]
-        // of chunk c's segment; eight loads in flight per thread
+        // gather + histogram: entry j of the concatenated segments is entry
+        // j - off[c] of chunk c's segment; eight loads in flight per thread
         constexpr int GB = 8;
         for (uint32_t base0 = 0; base0 < total; base0 += GB * kFinalThreads) {
             uint2 v[GB];
@@ -1228,20 +1300,71 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
 #pragma unroll
             for (int u = 0; u < GB; ++u) {
                 const uint32_t j = base0 + u * kFinalThreads + threadIdx.x;
-                if (j < total) cand[j] = v[u];
+                if (j < total) {
+                    cand[j] = v[u];
+                    atomicAdd(&hist[bin_of(Elem<DT>::key(v[u].x), t_lo, bin_shift)], 1u);
+                }
             }
         }
         __syncthreads();
-#pragma unroll
-        for (int j = 0; j < kBins / kFinalThreads; ++j) hist[threadIdx.x + j * kFinalThreads] = 0;
-        __syncthreads();
-        for (uint32_t j = threadIdx.x; j < total; j += blockDim.x)
-            atomicAdd(&hist[bin_of(Elem<DT>::key(cand[j].x), t_lo, bin_shift)], 1u);
-        __syncthreads();
         GBTOPK_TRACE_POINT(1, 0);
-        fallback = !select_from_candidates<DT, kFinalThreads>(PairSrc<DT>{cand}, total, hist, t_lo,
-                                                              bin_shift, k, det, sel, blist,
-                                                              kFinalBCap, c);
+        find_bin_from_top<kFinalThreads>(hist, static_cast<uint32_t>(k), c);
+        const uint32_t bstar = c.bcast[2], above = c.bcast[3], bsize = c.bcast[4];
+        if (bsize > static_cast<uint32_t>(kFinalBCap)) {
+            fallback = true;
+        } else {
+            // count-then-write: bins above b* go to sel, bin b* to blist
+            constexpr int CPT = kFinalCandCap / kFinalThreads;
+            uint32_t hi_mask = 0, eq_mask = 0, packed = 0;
+#pragma unroll
+            for (int u = 0; u < CPT; ++u) {
+                const uint32_t j = threadIdx.x + u * kFinalThreads;
+                if (j < total) {
+                    const uint32_t b = bin_of(Elem<DT>::key(cand[j].x), t_lo, bin_shift);
+                    hi_mask |= static_cast<uint32_t>(b > bstar) << u;
+                    eq_mask |= static_cast<uint32_t>(b == bstar) << u;
+                }
+            }
+            packed = (static_cast<uint32_t>(__popc(hi_mask)) << 16) | __popc(eq_mask);
+            uint32_t ptot;
+            const uint32_t pre = block_excl_scan(packed, c, ptot);
+            uint32_t hslot = pre >> 16, eslot = pre & 0xFFFFu;
+#pragma unroll
+            for (int u = 0; u < CPT; ++u) {
+                const uint32_t j = threadIdx.x + u * kFinalThreads;
+                if ((hi_mask >> u) & 1u) sel[hslot++] = cand[j];
+                if ((eq_mask >> u) & 1u) blist[eslot++] = cand[j];
+            }
+            __syncthreads();
+            const uint32_t need = static_cast<uint32_t>(k) - above;
+            if (bsize <= kRankMax) {
+                for (uint32_t i = threadIdx.x; i < bsize; i += blockDim.x) {
+                    const uint2 me = blist[i];
+                    const uint32_t mk = Elem<DT>::key(me.x);
+                    uint32_t rank = 0;
+                    for (uint32_t j2 = 0; j2 < bsize; ++j2) {
+                        const uint2 o = blist[j2];
+                        const uint32_t ok = Elem<DT>::key(o.x);
+                        rank += (ok > mk || (ok == mk && o.y < me.y)) ? 1u : 0u;
+                    }
+                    if (rank < need) sel[above + rank] = me;
+                }
+                __syncthreads();
+            } else {
+                constexpr int KB = Elem<DT>::kKeyBits;
+                const PairSrc<DT> bs{blist};
+                uint32_t t, gt;
+                block_select<KB, KB / 8>(bs, RankByKey{}, bsize, need, c.rhist, c, t, gt);
+                const uint32_t need_ties = need - gt;
+                uint32_t col_max = 0xFFFFFFFFu;
+                if (det) {
+                    uint32_t kk, g2;
+                    block_select<32, 4>(bs, RankTieColumn{t}, bsize, need_ties, c.rhist, c, kk, g2);
+                    col_max = ~kk;
+                }
+                collect<DT>(bs, bsize, t, gt, need_ties, det, col_max, sel, above, c);
+            }
+        }
     }
     if (fallback) exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, det, sel, c.rhist, c);
     GBTOPK_TRACE_POINT(2, 0);
@@ -1275,6 +1398,7 @@ cudaError_t launch_row(const Params &p, cudaStream_t stream) {
 // Row-kernel variant by the vectors each thread holds for a direct row.
 template <int DT>
 cudaError_t launch_row_any(const Params &p, cudaStream_t stream) {
+    if (p.plan.split) return launch_row<DT, 0>(p, stream);
     const int64_t vec = (static_cast<int64_t>(p.plan.direct_max) * Elem<DT>::kBytes + 16 + 15) / 16;
     if (vec <= 3 * kThreads) return launch_row<DT, 3>(p, stream);
     if (vec <= 9 * kThreads) return launch_row<DT, 9>(p, stream);

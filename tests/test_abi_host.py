@@ -133,7 +133,7 @@ def test_plan_totality_and_consistency():
         # a stream block and a row block must fit on one SM together
         assert p["row_smem"] + p["stream_smem"] + 2048 <= 228 * 1024
         if p["split"]:
-            assert W > p["direct_max"] == 2 * p["chunk"]
+            assert W > 2 * p["chunk"] and p["direct_max"] == k
             assert p["chunk"] * p["chunks_per_row"] >= W
             assert p["row_candidates"] >= k and p["ws_row_bytes"] >= 8 * p["row_candidates"]
         else:
