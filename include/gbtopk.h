@@ -173,6 +173,36 @@ int gbtopk_device_status(void *workspace, uint32_t *flags, void *stream);
 int gbtopk_plan_query(int64_t num_rows, int64_t width, int32_t top_k, int dtype,
                       int64_t *out);
 
+/*
+ * gbtopk_varlen_static_ws — gbtopk_varlen without a caller-provided
+ * workspace.  The pages define no such call; it exists for callers that
+ * cannot allocate device memory where they need top-K: code running while
+ * a CUDA graph is being captured (cudaMalloc cannot be captured), engines
+ * whose device memory belongs to an external allocator or planner that
+ * forbids side allocations, and plugin hosts that only pass in tensors they
+ * own.  It allocates nothing: the scratch is one 16 MiB buffer compiled into
+ * the library (a file-scope __device__ array), reserved on every GPU that
+ * loads the library and held until the process exits.
+ *
+ * Arguments, outputs and status codes are those of gbtopk_varlen, minus the
+ * workspace.  A geometry whose workspace (gbtopk_workspace_bytes) exceeds
+ * 16 MiB is refused with GBTOPK_EWORKSPACE before anything is enqueued; for
+ * example a 64 x 163840 fp32 batch with top_k 2048 needs about 6.3 MiB.
+ *
+ * The first call on a device looks up the buffer's device address (once per
+ * device); make that first call before capturing a CUDA graph.  All calls
+ * on a device share the one buffer and its contents carry over between
+ * calls (nothing needs clearing: each call writes the scratch it reads), so
+ * calls that may overlap in time on the GPU — other streams, concurrent
+ * graph replays, other host threads — race on it and must be serialised by
+ * the caller.
+ */
+int gbtopk_varlen_static_ws(const void *logits, int dtype, int64_t num_rows, int64_t width,
+                            int64_t row_stride, const int32_t *seq_lens, int32_t next_n,
+                            int32_t compress_ratio, int32_t top_k, const int32_t *pre_idx,
+                            int32_t *out_indices, void *out_values, int deterministic,
+                            void *stream);
+
 /* Human-readable name of a status code (static string). */
 const char *gbtopk_status_str(int status);
 

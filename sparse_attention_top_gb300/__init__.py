@@ -25,7 +25,8 @@ import torch
 __all__ = [
     "top_k_varlen", "top_k_page_table_transform", "gbtopk_varlen",
     "gbtopk_page_table_transform", "gbtopk_workspace_bytes", "gbtopk_device_status",
-    "gbtopk_plan_query", "gbtopk_status_str", "library_path", "load_library",
+    "gbtopk_plan_query", "gbtopk_status_str", "gbtopk_varlen_static_ws", "library_path",
+    "load_library",
     "GbtopkError", "MAX_TOP_K",
 ]
 
@@ -77,6 +78,9 @@ def load_library():
         lib.gbtopk_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
         lib.gbtopk_plan_query.restype = c_int
         lib.gbtopk_plan_query.argtypes = [i64, i64, i32, c_int, ctypes.POINTER(ctypes.c_int64)]
+        lib.gbtopk_varlen_static_ws.restype = c_int
+        lib.gbtopk_varlen_static_ws.argtypes = [vp, c_int, i64, i64, i64, vp, i32, i32, i32, vp, vp,
+                                                vp, c_int, vp]
         lib.gbtopk_status_str.restype = ctypes.c_char_p
         lib.gbtopk_status_str.argtypes = [c_int]
         _lib = lib
@@ -134,6 +138,21 @@ def gbtopk_varlen(logits: torch.Tensor, seq_lens: torch.Tensor, top_k: int,
         compress_ratio, top_k, _ptr(pre_idx), _ptr(out_indices), _ptr(out_values),
         1 if deterministic else 0, _ptr(workspace), workspace.numel() * workspace.element_size(),
         s))
+
+
+def gbtopk_varlen_static_ws(logits: torch.Tensor, seq_lens: torch.Tensor, top_k: int,
+                            pre_idx: Optional[torch.Tensor], next_n: int, compress_ratio: int,
+                            out_indices: torch.Tensor, out_values: Optional[torch.Tensor],
+                            deterministic: bool, stream=None) -> int:
+    """Direct call of the allocation-free variant (library-owned 16 MiB scratch
+    per GPU, shared by every call: serialise calls that could overlap)."""
+    R, W = logits.shape
+    stride = logits.stride(0) if R > 1 else W
+    s = _stream_handle(logits.device) if stream is None else stream
+    return _check(load_library().gbtopk_varlen_static_ws(
+        _ptr(logits), _DTYPES[logits.dtype], R, W, stride, _ptr(seq_lens), next_n,
+        compress_ratio, top_k, _ptr(pre_idx), _ptr(out_indices), _ptr(out_values),
+        1 if deterministic else 0, s))
 
 
 def gbtopk_page_table_transform(scores: torch.Tensor, lengths: torch.Tensor,

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libgbtopk.so")
-SOURCES = ["gbtopk_api.cu", "gbtopk_kernels.cu"]
+SOURCES = ["gbtopk_api.cu", "gbtopk_kernels.cu", "gbtopk_static_ws.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
