@@ -1231,19 +1231,38 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
 #endif
 }
 
-// Finalize kernel: one block per split row gathers the row's chunk segments
-// into shared memory, histograms the candidates' keys, and selects the exact
-// top-k (falling back to an exact radix select over the row in global memory
-// when a segment overflowed or the guess was too high).
+// Finalize kernel: one block per split row.  Two passes over the row's
+// chunk segments (L2-resident): the first histograms the candidates' keys,
+// the second keeps every candidate above the boundary bin and collects the
+// boundary bin's members, which are then ranked exactly.  Falls back to an
+// exact radix select over the row in global memory when a segment
+// overflowed, the guess was too high or the boundary bin is too crowded.
+struct SegMap {  // candidate j of the concatenated segments -> its address
+    const uint2 *segs;
+    const uint32_t *choff;  // first candidate number of each chunk
+    int nch;
+    uint32_t cap;
+    __device__ __forceinline__ const uint2 *at(uint32_t j) const {
+        int lo = 0, hi = nch - 1;  // last chunk with choff <= j
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (choff[mid] <= j) lo = mid;
+            else hi = mid - 1;
+        }
+        return segs + static_cast<int64_t>(lo) * cap + (j - choff[lo]);
+    }
+};
+
 template <int DT>
 __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_constant__ Params p) {
     using raw_t = typename Elem<DT>::raw_t;
+    constexpr int GB = 8;  // candidates in flight per thread
     extern __shared__ __align__(128) uint8_t smem[];
     Ctrl &c = *reinterpret_cast<Ctrl *>(smem);
     uint32_t *hist = reinterpret_cast<uint32_t *>(smem + kCtrlBytes);
     uint2 *sel = reinterpret_cast<uint2 *>(smem + kCtrlBytes);  // aliases hist
-    uint2 *cand = reinterpret_cast<uint2 *>(smem + kCtrlBytes + kFinalHistBytes);
-    uint2 *blist = cand + kFinalCandCap;
+    uint2 *blist = reinterpret_cast<uint2 *>(smem + kCtrlBytes + kFinalHistBytes);
+    uint32_t *choff = reinterpret_cast<uint32_t *>(blist + kFinalBCap);
     const int64_t row = p.row0 + blockIdx.x;
     const int k = p.k;
     const bool det = p.deterministic != 0;
@@ -1261,49 +1280,33 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
     const int bin_shift = static_cast<int>(__ldcg(info + 1));
     const uint32_t cap = static_cast<uint32_t>(chunk_seg_cap(n, k, p.plan.chunk));
     const uint32_t *counts = row_counts(p, row);
-    const uint2 *segs = row_segs(p, row);
 
     // chunk counts -> offsets (nch <= kFinalThreads, checked on the host)
     const uint32_t my = threadIdx.x < nch ? __ldcg(counts + threadIdx.x) : 0u;
     if (threadIdx.x == 0) c.bcast[5] = 0;
+#pragma unroll
+    for (int j = 0; j < kBins / kFinalThreads; ++j) hist[threadIdx.x + j * kFinalThreads] = 0;
     __syncthreads();
     if (my > cap) atomicOr(&c.bcast[5], 1u);
     uint32_t total;
     const uint32_t base = block_excl_scan(my > cap ? 0u : my, c, total);
-    bool fallback = c.bcast[5] != 0 || total < static_cast<uint32_t>(k) ||
-                    total > static_cast<uint32_t>(kFinalCandCap);
+    if (threadIdx.x < nch) choff[threadIdx.x] = base;
+    bool fallback = c.bcast[5] != 0 || total < static_cast<uint32_t>(k);
+    __syncthreads();
+    const SegMap map{row_segs(p, row), choff, static_cast<int>(nch), cap};
     if (!fallback) {
-        uint32_t *choff = reinterpret_cast<uint32_t *>(blist);  // chunk offsets (blist is free yet)
-        if (threadIdx.x < nch) choff[threadIdx.x] = base;
-#pragma unroll
-        for (int j = 0; j < kBins / kFinalThreads; ++j) hist[threadIdx.x + j * kFinalThreads] = 0;
-        __syncthreads();
-        // gather + histogram: entry j of the concatenated segments is entry
-        // j - off[c] of chunk c's segment; eight loads in flight per thread
-        constexpr int GB = 8;
-        for (uint32_t base0 = 0; base0 < total; base0 += GB * kFinalThreads) {
-            uint2 v[GB];
+        // pass 1: histogram of the candidates' keys
+        for (uint32_t b0 = 0; b0 < total; b0 += GB * kFinalThreads) {
+            uint32_t raw[GB];
 #pragma unroll
             for (int u = 0; u < GB; ++u) {
-                const uint32_t j = base0 + u * kFinalThreads + threadIdx.x;
-                v[u] = make_uint2(0, 0);
-                if (j < total) {
-                    int lo = 0, hi = static_cast<int>(nch) - 1;  // last chunk with off <= j
-                    while (lo < hi) {
-                        const int mid = (lo + hi + 1) >> 1;
-                        if (choff[mid] <= j) lo = mid;
-                        else hi = mid - 1;
-                    }
-                    v[u] = __ldcg(segs + static_cast<int64_t>(lo) * cap + (j - choff[lo]));
-                }
+                const uint32_t j = b0 + u * kFinalThreads + threadIdx.x;
+                raw[u] = j < total ? __ldcg(map.at(j)).x : 0u;
             }
 #pragma unroll
             for (int u = 0; u < GB; ++u) {
-                const uint32_t j = base0 + u * kFinalThreads + threadIdx.x;
-                if (j < total) {
-                    cand[j] = v[u];
-                    atomicAdd(&hist[bin_of(Elem<DT>::key(v[u].x), t_lo, bin_shift)], 1u);
-                }
+                const uint32_t j = b0 + u * kFinalThreads + threadIdx.x;
+                if (j < total) atomicAdd(&hist[bin_of(Elem<DT>::key(raw[u]), t_lo, bin_shift)], 1u);
             }
         }
         __syncthreads();
@@ -1313,27 +1316,36 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
         if (bsize > static_cast<uint32_t>(kFinalBCap)) {
             fallback = true;
         } else {
-            // count-then-write: bins above b* go to sel, bin b* to blist
-            constexpr int CPT = kFinalCandCap / kFinalThreads;
-            uint32_t hi_mask = 0, eq_mask = 0, packed = 0;
+            // pass 2: bins above b* go to sel, bin b* to blist (count-then-write per batch)
+            uint32_t hi_base = 0, eq_base = 0;
+            for (uint32_t b0 = 0; b0 < total; b0 += GB * kFinalThreads) {
+                uint2 v[GB];
+                uint32_t hi_mask = 0, eq_mask = 0;
 #pragma unroll
-            for (int u = 0; u < CPT; ++u) {
-                const uint32_t j = threadIdx.x + u * kFinalThreads;
-                if (j < total) {
-                    const uint32_t b = bin_of(Elem<DT>::key(cand[j].x), t_lo, bin_shift);
-                    hi_mask |= static_cast<uint32_t>(b > bstar) << u;
-                    eq_mask |= static_cast<uint32_t>(b == bstar) << u;
+                for (int u = 0; u < GB; ++u) {
+                    const uint32_t j = b0 + u * kFinalThreads + threadIdx.x;
+                    v[u] = j < total ? __ldcg(map.at(j)) : make_uint2(0, 0);
                 }
-            }
-            packed = (static_cast<uint32_t>(__popc(hi_mask)) << 16) | __popc(eq_mask);
-            uint32_t ptot;
-            const uint32_t pre = block_excl_scan(packed, c, ptot);
-            uint32_t hslot = pre >> 16, eslot = pre & 0xFFFFu;
 #pragma unroll
-            for (int u = 0; u < CPT; ++u) {
-                const uint32_t j = threadIdx.x + u * kFinalThreads;
-                if ((hi_mask >> u) & 1u) sel[hslot++] = cand[j];
-                if ((eq_mask >> u) & 1u) blist[eslot++] = cand[j];
+                for (int u = 0; u < GB; ++u) {
+                    const uint32_t j = b0 + u * kFinalThreads + threadIdx.x;
+                    if (j < total) {
+                        const uint32_t b = bin_of(Elem<DT>::key(v[u].x), t_lo, bin_shift);
+                        hi_mask |= static_cast<uint32_t>(b > bstar) << u;
+                        eq_mask |= static_cast<uint32_t>(b == bstar) << u;
+                    }
+                }
+                const uint32_t packed = (static_cast<uint32_t>(__popc(hi_mask)) << 16) | __popc(eq_mask);
+                uint32_t ptot;
+                const uint32_t pre = block_excl_scan(packed, c, ptot);
+                uint32_t hs = hi_base + (pre >> 16), es = eq_base + (pre & 0xFFFFu);
+#pragma unroll
+                for (int u = 0; u < GB; ++u) {
+                    if ((hi_mask >> u) & 1u) sel[hs++] = v[u];
+                    if ((eq_mask >> u) & 1u) blist[es++] = v[u];
+                }
+                hi_base += ptot >> 16;
+                eq_base += ptot & 0xFFFFu;
             }
             __syncthreads();
             const uint32_t need = static_cast<uint32_t>(k) - above;
