@@ -836,8 +836,9 @@ __device__ __forceinline__ int64_t split_chunks(const Params &p, int64_t n) {
 // in the row's workspace for the stream and finalize kernels.  It releases
 // the dependent stream kernel (programmatic dependent launch) once its own
 // global loads are in, so the stream's bulk copies do not queue ahead of them.
+// Narrow variants (VPT <= 3) keep to 64 registers so four blocks share an SM.
 template <int DT, int VPT>
-__global__ void __launch_bounds__(kThreads) row_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const __grid_constant__ Params p) {
     using raw_t = typename Elem<DT>::raw_t;
     extern __shared__ __align__(128) uint8_t smem[];
     Ctrl &c = *reinterpret_cast<Ctrl *>(smem);
