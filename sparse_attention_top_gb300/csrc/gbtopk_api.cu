@@ -64,8 +64,10 @@ int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *p
         pl.block_rows = num_rows < kMaxBlockRows ? num_rows : kMaxBlockRows;
         pl.stream_smem = kCtrlBytes + align_up(static_cast<size_t>(kMaxBlockRows + 1) * 16, 128) +
                          static_cast<size_t>(kStages) * kStageBytes;
-        pl.final_smem = kCtrlBytes + kFinalHistBytes + static_cast<size_t>(kFinalBCap) * sizeof(uint2) +
-                        4 * static_cast<size_t>(kFinalThreads);
+        // finalize: control, histogram / selection, boundary bin, chunk
+        // offsets, then the gathered candidates (kGatherCandidates)
+        pl.final_smem = kCtrlBytes + kFinalHistBytes + static_cast<size_t>(kFinalBCap) * 8 +
+                        4 * static_cast<size_t>(kFinalThreads) + static_cast<size_t>(kGatherCandidates) * 8;
         // candidate entries per row: the largest chunks x per-chunk capacity
         // over the row lengths the width allows (capacity shrinks as n grows,
         // so within a chunk count the shortest row is the worst case)

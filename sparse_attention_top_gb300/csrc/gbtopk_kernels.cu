@@ -1232,47 +1232,59 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
 #endif
 }
 
-// Finalize kernel: one block per split row.  Two passes over the row's
-// chunk segments (L2-resident): the first histograms the candidates' keys,
-// the second keeps every candidate above the boundary bin and collects the
-// boundary bin's members, which are then ranked exactly.  Falls back to an
-// exact radix select over the row in global memory when a segment
-// overflowed, the guess was too high or the boundary bin is too crowded.
+// Finalize kernel: one block per split row.  The row's chunk segments
+// (L2-resident) are gathered into shared memory by one bulk copy per chunk
+// (each segment padded to an even count so every copy starts on a 16-byte
+// boundary; the padding slot is marked with column 0xFFFFFFFF), then the
+// candidates' keys are histogrammed over kBins bins above the guess, the bin
+// holding the k-th key is found, every candidate of a higher bin is kept and
+// the boundary bin's members are ranked exactly.  Rows with more candidates
+// than the shared buffer holds make the same two passes straight over the
+// segments in L2.  Falls back to an exact radix select over the row in
+// global memory when a segment overflowed, the guess was too high or the
+// boundary bin is too crowded.
 struct SegMap {  // candidate j of the concatenated segments -> its address
     const uint2 *segs;
     const uint32_t *choff;  // first candidate number of each chunk
     int nch;
     uint32_t cap;
-    __device__ __forceinline__ const uint2 *at(uint32_t j) const {
-        int lo = 0, hi = nch - 1;  // last chunk with choff <= j
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (choff[mid] <= j) lo = mid;
-            else hi = mid - 1;
-        }
-        return segs + static_cast<int64_t>(lo) * cap + (j - choff[lo]);
+    // `ch` is a cursor the caller keeps: each thread visits increasing j
+    __device__ __forceinline__ const uint2 *at(uint32_t j, int &ch) const {
+        while (ch + 1 < nch && choff[ch + 1] <= j) ++ch;
+        return segs + static_cast<int64_t>(ch) * cap + (j - choff[ch]);
     }
 };
+
+constexpr uint32_t kPadColumn = 0xFFFFFFFFu;  // marks a gather padding slot
 
 template <int DT>
 __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_constant__ Params p) {
     using raw_t = typename Elem<DT>::raw_t;
-    constexpr int GB = 8;  // candidates in flight per thread
+    constexpr int GB = 8;  // candidates in flight per thread (L2 path)
     extern __shared__ __align__(128) uint8_t smem[];
     Ctrl &c = *reinterpret_cast<Ctrl *>(smem);
     uint32_t *hist = reinterpret_cast<uint32_t *>(smem + kCtrlBytes);
     uint2 *sel = reinterpret_cast<uint2 *>(smem + kCtrlBytes);  // aliases hist
     uint2 *blist = reinterpret_cast<uint2 *>(smem + kCtrlBytes + kFinalHistBytes);
     uint32_t *choff = reinterpret_cast<uint32_t *>(blist + kFinalBCap);
+    uint2 *cand = reinterpret_cast<uint2 *>(choff + kFinalThreads);  // gathered candidates
+    const uint32_t gather_cap = static_cast<uint32_t>(
+        (p.plan.final_smem - (kCtrlBytes + kFinalHistBytes + static_cast<size_t>(kFinalBCap) * 8 +
+                              4 * static_cast<size_t>(kFinalThreads))) / sizeof(uint2));
     const int64_t row = p.row0 + blockIdx.x;
     const int k = p.k;
     const bool det = p.deterministic != 0;
+    const int tid = threadIdx.x;
     constexpr int kTraceBase = 40960;
     (void)kTraceBase;
     int64_t n, col0;
     row_window(p, row, n, col0);
     const int64_t nch = split_chunks(p, n);
     if (nch == 0) return;
+    if (tid == 0) {
+        mbar_init(&c.bar);
+        c.bcast[5] = 0;
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     GBTOPK_TRACE_POINT(0, 0);
     const raw_t *xrow = static_cast<const raw_t *>(p.x) + row * p.row_stride + col0;
@@ -1280,57 +1292,149 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
     const uint32_t t_lo = __ldcg(info);
     const int bin_shift = static_cast<int>(__ldcg(info + 1));
     const uint32_t cap = static_cast<uint32_t>(chunk_seg_cap(n, k, p.plan.chunk));
-    const uint32_t *counts = row_counts(p, row);
+    const uint2 *segs = row_segs(p, row);
 
-    // chunk counts -> offsets (nch <= kFinalThreads, checked on the host)
-    const uint32_t my = threadIdx.x < nch ? __ldcg(counts + threadIdx.x) : 0u;
-    if (threadIdx.x == 0) c.bcast[5] = 0;
+    // chunk counts -> padded offsets (nch <= kFinalThreads, checked on the host)
+    const uint32_t my = tid < nch ? __ldcg(row_counts(p, row) + tid) : 0u;
 #pragma unroll
-    for (int j = 0; j < kBins / kFinalThreads; ++j) hist[threadIdx.x + j * kFinalThreads] = 0;
-    __syncthreads();
-    if (my > cap) atomicOr(&c.bcast[5], 1u);
-    uint32_t total;
-    const uint32_t base = block_excl_scan(my > cap ? 0u : my, c, total);
-    if (threadIdx.x < nch) choff[threadIdx.x] = base;
+    for (int j = 0; j < kBins / kFinalThreads; ++j) hist[tid + j * kFinalThreads] = 0;
+    const bool over = my > cap;
+    const uint32_t cnt = over ? 0u : my;
+    const uint32_t padded = (cnt + 1u) & ~1u;
+    if (over) atomicOr(&c.bcast[5], 1u);
+    const int odd = __syncthreads_count(cnt & 1u);
+    uint32_t total_p;
+    const uint32_t poff = block_excl_scan(padded, c, total_p);
+    const uint32_t total = total_p - static_cast<uint32_t>(odd);
     bool fallback = c.bcast[5] != 0 || total < static_cast<uint32_t>(k);
-    __syncthreads();
-    const SegMap map{row_segs(p, row), choff, static_cast<int>(nch), cap};
-    if (!fallback) {
-        // pass 1: histogram of the candidates' keys
+    const bool in_smem = total_p <= gather_cap;
+    bool copy_ok = true;
+    if (!fallback && in_smem) {
+        // ---- gather the segments into shared memory (one bulk copy per chunk)
+        if (tid == 0) {
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&c.bar)),
+                         "r"(total_p * 8u)
+                         : "memory");
+        }
+        __syncthreads();
+        if (tid < nch && padded > 0) {
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    smem_u32(cand + poff)),
+                "l"(segs + static_cast<int64_t>(tid) * cap), "r"(padded * 8u), "r"(smem_u32(&c.bar))
+                : "memory");
+        }
+        copy_ok = wait_bar(p.ws, c, &c.bar, 0);
+        if (copy_ok) {
+            if (tid < nch && (cnt & 1u)) cand[poff + cnt].y = kPadColumn;
+            __syncthreads();
+            GBTOPK_TRACE_POINT(1, 0);
+            for (uint32_t i = tid; i < total_p; i += kFinalThreads) {
+                const uint2 v = cand[i];
+                if (v.y != kPadColumn) atomicAdd(&hist[bin_of(Elem<DT>::key(v.x), t_lo, bin_shift)], 1u);
+            }
+            __syncthreads();
+            find_bin_from_top<kFinalThreads>(hist, static_cast<uint32_t>(k), c);
+            const uint32_t bstar = c.bcast[2], above = c.bcast[3], bsize = c.bcast[4];
+            if (bsize > static_cast<uint32_t>(kFinalBCap)) {
+                fallback = true;
+            } else {
+                if (tid == 0) {
+                    c.sel_count = 0;
+                    c.b_count = 0;
+                }
+                __syncthreads();
+                // bins above b* go to sel, bin b* to blist (sel aliases the consumed histogram)
+                for (uint32_t i0 = 0; i0 < total_p; i0 += kFinalThreads) {
+                    const uint32_t i = i0 + tid;
+                    uint2 v = make_uint2(0, kPadColumn);
+                    if (i < total_p) v = cand[i];
+                    const bool live = v.y != kPadColumn;
+                    const uint32_t b = bin_of(Elem<DT>::key(v.x), t_lo, bin_shift);
+                    const bool hi = live && b > bstar, eq = live && b == bstar;
+                    const uint32_t hs = warp_claim(&c.sel_count, hi);
+                    if (hi) sel[hs] = v;
+                    const uint32_t es = warp_claim(&c.b_count, eq);
+                    if (eq) blist[es] = v;
+                }
+                __syncthreads();
+                GBTOPK_TRACE_POINT(3, 0);
+                const uint32_t need = static_cast<uint32_t>(k) - above;
+                if (bsize <= kRankMax) {
+                    for (uint32_t i = tid; i < bsize; i += kFinalThreads) {
+                        const uint2 me = blist[i];
+                        const uint32_t mk = Elem<DT>::key(me.x);
+                        uint32_t rank = 0;
+                        for (uint32_t j2 = 0; j2 < bsize; ++j2) {
+                            const uint2 o = blist[j2];
+                            const uint32_t ok = Elem<DT>::key(o.x);
+                            rank += (ok > mk || (ok == mk && o.y < me.y)) ? 1u : 0u;
+                        }
+                        if (rank < need) sel[above + rank] = me;
+                    }
+                    __syncthreads();
+                } else {
+                    constexpr int KB = Elem<DT>::kKeyBits;
+                    const PairSrc<DT> bs{blist};
+                    uint32_t t, gt;
+                    block_select<KB, KB / 8>(bs, RankByKey{}, bsize, need, c.rhist, c, t, gt);
+                    const uint32_t need_ties = need - gt;
+                    uint32_t col_max = 0xFFFFFFFFu;
+                    if (det) {
+                        uint32_t kk, g2;
+                        block_select<32, 4>(bs, RankTieColumn{t}, bsize, need_ties, c.rhist, c, kk, g2);
+                        col_max = ~kk;
+                    }
+                    collect<DT>(bs, bsize, t, gt, need_ties, det, col_max, sel, above, c);
+                }
+            }
+        } else {
+            fallback = true;
+        }
+    } else if (!fallback) {
+        // ---- two passes straight over the segments in L2 (unpadded offsets)
+        const uint32_t base = block_excl_scan(cnt, c, total_p);
+        if (tid < nch) choff[tid] = base;
+        __syncthreads();
+        const SegMap map{segs, choff, static_cast<int>(nch), cap};
+        int cur = 0;
         for (uint32_t b0 = 0; b0 < total; b0 += GB * kFinalThreads) {
+            const uint2 *addr[GB];
             uint32_t raw[GB];
 #pragma unroll
             for (int u = 0; u < GB; ++u) {
-                const uint32_t j = b0 + u * kFinalThreads + threadIdx.x;
-                raw[u] = j < total ? __ldcg(map.at(j)).x : 0u;
+                const uint32_t j = b0 + u * kFinalThreads + tid;
+                addr[u] = j < total ? map.at(j, cur) : nullptr;
             }
 #pragma unroll
-            for (int u = 0; u < GB; ++u) {
-                const uint32_t j = b0 + u * kFinalThreads + threadIdx.x;
-                if (j < total) atomicAdd(&hist[bin_of(Elem<DT>::key(raw[u]), t_lo, bin_shift)], 1u);
-            }
+            for (int u = 0; u < GB; ++u) raw[u] = addr[u] ? __ldcg(addr[u]).x : 0u;
+#pragma unroll
+            for (int u = 0; u < GB; ++u)
+                if (addr[u]) atomicAdd(&hist[bin_of(Elem<DT>::key(raw[u]), t_lo, bin_shift)], 1u);
         }
         __syncthreads();
-        GBTOPK_TRACE_POINT(1, 0);
         find_bin_from_top<kFinalThreads>(hist, static_cast<uint32_t>(k), c);
         const uint32_t bstar = c.bcast[2], above = c.bcast[3], bsize = c.bcast[4];
         if (bsize > static_cast<uint32_t>(kFinalBCap)) {
             fallback = true;
         } else {
-            // pass 2: bins above b* go to sel, bin b* to blist (count-then-write per batch)
+            // bins above b* go to sel, bin b* to blist (count-then-write per batch)
             uint32_t hi_base = 0, eq_base = 0;
+            int cur2 = 0;
             for (uint32_t b0 = 0; b0 < total; b0 += GB * kFinalThreads) {
+                const uint2 *addr[GB];
                 uint2 v[GB];
                 uint32_t hi_mask = 0, eq_mask = 0;
 #pragma unroll
                 for (int u = 0; u < GB; ++u) {
-                    const uint32_t j = b0 + u * kFinalThreads + threadIdx.x;
-                    v[u] = j < total ? __ldcg(map.at(j)) : make_uint2(0, 0);
+                    const uint32_t j = b0 + u * kFinalThreads + tid;
+                    addr[u] = j < total ? map.at(j, cur2) : nullptr;
                 }
 #pragma unroll
+                for (int u = 0; u < GB; ++u) v[u] = addr[u] ? __ldcg(addr[u]) : make_uint2(0, 0);
+#pragma unroll
                 for (int u = 0; u < GB; ++u) {
-                    const uint32_t j = b0 + u * kFinalThreads + threadIdx.x;
-                    if (j < total) {
+                    if (addr[u]) {
                         const uint32_t b = bin_of(Elem<DT>::key(v[u].x), t_lo, bin_shift);
                         hi_mask |= static_cast<uint32_t>(b > bstar) << u;
                         eq_mask |= static_cast<uint32_t>(b == bstar) << u;
@@ -1351,7 +1455,7 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
             __syncthreads();
             const uint32_t need = static_cast<uint32_t>(k) - above;
             if (bsize <= kRankMax) {
-                for (uint32_t i = threadIdx.x; i < bsize; i += blockDim.x) {
+                for (uint32_t i = tid; i < bsize; i += kFinalThreads) {
                     const uint2 me = blist[i];
                     const uint32_t mk = Elem<DT>::key(me.x);
                     uint32_t rank = 0;
@@ -1383,8 +1487,9 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
     GBTOPK_TRACE_POINT(2, 0);
     if (det) sort_selection<DT>(sel, k);
     emit<DT>(p, row, sel, k);
+    if (!copy_ok && tid == 0) mbar_wait(&c.bar, 0);  // let the copies land before exit
     GBTOPK_TRACE_POINT(6, 0);
-    GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | (fallback ? 5u : 4u) |
+    GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | (fallback ? 5u : (in_smem ? 4u : 3u)) |
                               (static_cast<unsigned long long>(total) << 40));
 }
 
