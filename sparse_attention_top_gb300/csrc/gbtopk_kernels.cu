@@ -50,9 +50,21 @@ __device__ unsigned long long g_trace[kTraceBlocks][16];
             g_trace[kTraceBase + blockIdx.x][slot] = ((slot) == 7 || (slot) == 15) ? (value) : t_; \
         }                                                                                    \
     } while (0)
+// g_trace[index][slot] = the current time (value < 0) or value, from any thread.
+#define GBTOPK_TRACE_SET(index, slot, value)                                              \
+    do {                                                                                 \
+        if ((index) < kTraceBlocks) {                                                    \
+            long long v_ = (value);                                                      \
+            if (v_ < 0) asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(v_));          \
+            g_trace[(index)][(slot)] = static_cast<unsigned long long>(v_);              \
+        }                                                                                \
+    } while (0)
 #else
 #define GBTOPK_TRACE_POINT(slot, value) \
     do {                                \
+    } while (0)
+#define GBTOPK_TRACE_SET(index, slot, value) \
+    do {                                     \
     } while (0)
 #endif
 
@@ -867,6 +879,12 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
         // row when it has at most kSampleSize columns)
         int m;
         uint32_t kmin = 0xFFFFFFFFu, kmax = 0;
+        // hint anchor (the previous argmax column): thread 32 issues its two
+        // dependent loads alongside the sample's, and folds the value in
+        // after the barrier
+        constexpr int kHintThread = 32;
+        int32_t a = -1;
+        if (threadIdx.x == kHintThread && p.pre_idx) a = __ldg(p.pre_idx + (row / p.next_n) * k);
         if (n > kSampleSize) {
             m = kSampleSize;
             const int64_t pos = static_cast<int64_t>(threadIdx.x) * (n - 8) / (kSampleGroups - 1);
@@ -889,16 +907,19 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
                 kmax = key > kmax ? key : kmax;
             }
         }
+        const bool hint_ok = threadIdx.x == kHintThread &&
+                             static_cast<uint64_t>(static_cast<uint32_t>(a)) < static_cast<uint64_t>(n);
+        uint32_t hraw = 0;
+        if (hint_ok) hraw = ldg_raw(xrow + a);
         __syncthreads();
+        GBTOPK_TRACE_POINT(1, 0);
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-        if (threadIdx.x == 0 && p.pre_idx) {  // hint anchor: previous argmax column
-            const int32_t a = __ldg(p.pre_idx + (row / p.next_n) * k);
-            if (static_cast<uint64_t>(static_cast<uint32_t>(a)) < static_cast<uint64_t>(n)) {
-                const uint32_t key = Elem<DT>::key(ldg_raw(xrow + a));
-                kmax = key > kmax ? key : kmax;
-            }
+        if (hint_ok) {
+            const uint32_t key = Elem<DT>::key(hraw);
+            kmax = key > kmax ? key : kmax;
         }
         block_minmax(kmin, kmax, c);
+        GBTOPK_TRACE_POINT(2, 0);
         uint32_t t_lo;
         int bin_shift;
         guess_from_sample<kThreads>(sample, m, n, k, c.key_min, c.key_max, hist, c, t_lo, bin_shift);
@@ -1004,6 +1025,7 @@ struct RowFacts {
     uint32_t t_lo;     // threshold guess (after the row kernel)
 };
 static_assert(sizeof(RowFacts) == 16, "row facts");
+static_assert(sizeof(Ctrl) + kStages * sizeof(StageMeta) <= kCtrlBytes, "stage metadata after the control block");
 
 __device__ __forceinline__ void mbar_init_count(unsigned long long *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -1257,6 +1279,168 @@ struct SegMap {  // candidate j of the concatenated segments -> its address
 
 constexpr uint32_t kPadColumn = 0xFFFFFFFFu;  // marks a gather padding slot
 
+// Completes sel[above, above + need) with the best `need` of the bsize
+// members of the boundary bin (blist), ranked by (key desc, column asc).
+template <int DT, int NT>
+__device__ bool rank_boundary(const uint2 *blist, uint32_t bsize, uint32_t need, uint32_t above, bool det,
+                              uint2 *sel, Ctrl &c) {
+    const uint32_t tid = threadIdx.x;
+    if (bsize <= kRankMax) {
+        // one warp per member of bin b*: its rank among the others, counted across the lanes
+        const uint32_t w = tid >> 5, lane = lane_id();
+        for (uint32_t i = w; i < bsize; i += NT / 32) {
+            const uint2 me = blist[i];
+            const uint32_t mk = Elem<DT>::key(me.x);
+            uint32_t rank = 0;
+            for (uint32_t j2 = lane; j2 < bsize; j2 += 32) {
+                const uint2 o = blist[j2];
+                const uint32_t ok = Elem<DT>::key(o.x);
+                rank += (ok > mk || (ok == mk && o.y < me.y)) ? 1u : 0u;
+            }
+            rank = __reduce_add_sync(0xffffffffu, rank);
+            if (lane == 0 && rank < need) sel[above + rank] = me;
+        }
+        __syncthreads();
+    } else {
+        constexpr int KB = Elem<DT>::kKeyBits;
+        const PairSrc<DT> bs{blist};
+        uint32_t t, gt;
+        block_select<KB, KB / 8>(bs, RankByKey{}, bsize, need, c.rhist, c, t, gt);
+        const uint32_t need_ties = need - gt;
+        uint32_t col_max = 0xFFFFFFFFu;
+        if (det) {
+            uint32_t kk, g2;
+            block_select<32, 4>(bs, RankTieColumn{t}, bsize, need_ties, c.rhist, c, kk, g2);
+            col_max = ~kk;
+        }
+        collect<DT>(bs, bsize, t, gt, need_ties, det, col_max, sel, above, c);
+    }
+    return true;
+}
+
+// Exact top-k among candidates gathered in shared memory: cand[0, total_p)
+// holds (raw, column) pairs, padding slots carry column kPadColumn, every
+// live candidate has key >= t_lo and at least k are live.  The keys are
+// histogrammed over kBins bins (bin_of), the bin b* holding the k-th key
+// from the top is found, the candidates of higher bins go to sel and b*'s
+// members to blist, ranked by (key desc, column asc) so the best `need`
+// complete sel[0, k).  `sel` may alias `hist`.  All NT threads of the block
+// call it; returns false (nothing written) when b* holds more than
+// kFinalBCap members.
+template <int DT, int NT>
+__device__ bool select_gathered(const uint2 *cand, uint32_t total_p, uint32_t t_lo, int bin_shift, int k,
+                                bool det, uint32_t *hist, uint2 *sel, uint2 *blist, Ctrl &c) {
+    const uint32_t tid = threadIdx.x;
+#pragma unroll
+    for (int j = 0; j < kBins / NT; ++j) hist[tid + j * NT] = 0;
+    __syncthreads();
+    for (uint32_t i = tid; i < total_p; i += NT) {
+        const uint2 v = cand[i];
+        if (v.y != kPadColumn) atomicAdd(&hist[bin_of(Elem<DT>::key(v.x), t_lo, bin_shift)], 1u);
+    }
+    __syncthreads();
+    find_bin_from_top<NT>(hist, static_cast<uint32_t>(k), c);
+    const uint32_t bstar = c.bcast[2], above = c.bcast[3], bsize = c.bcast[4];
+    if (bsize > static_cast<uint32_t>(kFinalBCap)) return false;
+    // bins above b* go to sel, bin b* to blist (sel aliases the consumed
+    // histogram): each thread counts its candidates (a contiguous run), one
+    // block scan gives its output slots
+    const uint32_t per = (total_p + NT - 1) / NT;
+    const uint32_t i_lo = tid * per < total_p ? tid * per : total_p;
+    const uint32_t i_hi = i_lo + per < total_p ? i_lo + per : total_p;
+    uint32_t nhi = 0, neq = 0;
+    for (uint32_t i = i_lo; i < i_hi; ++i) {
+        const uint2 v = cand[i];
+        const uint32_t b = bin_of(Elem<DT>::key(v.x), t_lo, bin_shift);
+        const bool live = v.y != kPadColumn;
+        nhi += (live && b > bstar) ? 1u : 0u;
+        neq += (live && b == bstar) ? 1u : 0u;
+    }
+    uint32_t ptot;
+    const uint32_t pre = block_excl_scan((nhi << 16) | neq, c, ptot);
+    uint32_t hs = pre >> 16, es = pre & 0xFFFFu;
+    for (uint32_t i = i_lo; i < i_hi && (nhi | neq); ++i) {
+        const uint2 v = cand[i];
+        if (v.y == kPadColumn) continue;
+        const uint32_t b = bin_of(Elem<DT>::key(v.x), t_lo, bin_shift);
+        if (b > bstar) sel[hs++] = v;
+        else if (b == bstar) blist[es++] = v;
+    }
+    __syncthreads();
+    return rank_boundary<DT, NT>(blist, bsize, static_cast<uint32_t>(k) - above, above, det, sel, c);
+}
+
+// Exact top-k among `total` (>= k) candidates left in workspace segments
+// (L2-resident; `map` numbers them consecutively), for rows whose
+// candidates do not fit in shared memory: two passes over the segments, the
+// first histogramming the keys, the second keeping the bins above the
+// boundary bin and collecting its members, which are ranked exactly.  Same
+// contract as select_gathered.
+template <int DT, int NT>
+__device__ bool select_from_segments(const SegMap &map, uint32_t total, uint32_t t_lo, int bin_shift, int k,
+                                     bool det, uint32_t *hist, uint2 *sel, uint2 *blist, Ctrl &c) {
+    constexpr int GB = 8;  // candidates in flight per thread
+    const uint32_t tid = threadIdx.x;
+#pragma unroll
+    for (int j = 0; j < kBins / NT; ++j) hist[tid + j * NT] = 0;
+    __syncthreads();
+    int cur = 0;
+    for (uint32_t b0 = 0; b0 < total; b0 += GB * NT) {
+        const uint2 *addr[GB];
+        uint32_t raw[GB];
+#pragma unroll
+        for (int u = 0; u < GB; ++u) {
+            const uint32_t j = b0 + u * NT + tid;
+            addr[u] = j < total ? map.at(j, cur) : nullptr;
+        }
+#pragma unroll
+        for (int u = 0; u < GB; ++u) raw[u] = addr[u] ? __ldcg(addr[u]).x : 0u;
+#pragma unroll
+        for (int u = 0; u < GB; ++u)
+            if (addr[u]) atomicAdd(&hist[bin_of(Elem<DT>::key(raw[u]), t_lo, bin_shift)], 1u);
+    }
+    __syncthreads();
+    find_bin_from_top<NT>(hist, static_cast<uint32_t>(k), c);
+    const uint32_t bstar = c.bcast[2], above = c.bcast[3], bsize = c.bcast[4];
+    if (bsize > static_cast<uint32_t>(kFinalBCap)) return false;
+    // bins above b* go to sel, bin b* to blist (count-then-write per batch)
+    uint32_t hi_base = 0, eq_base = 0;
+    int cur2 = 0;
+    for (uint32_t b0 = 0; b0 < total; b0 += GB * NT) {
+        const uint2 *addr[GB];
+        uint2 v[GB];
+        uint32_t hi_mask = 0, eq_mask = 0;
+#pragma unroll
+        for (int u = 0; u < GB; ++u) {
+            const uint32_t j = b0 + u * NT + tid;
+            addr[u] = j < total ? map.at(j, cur2) : nullptr;
+        }
+#pragma unroll
+        for (int u = 0; u < GB; ++u) v[u] = addr[u] ? __ldcg(addr[u]) : make_uint2(0, 0);
+#pragma unroll
+        for (int u = 0; u < GB; ++u) {
+            if (addr[u]) {
+                const uint32_t b = bin_of(Elem<DT>::key(v[u].x), t_lo, bin_shift);
+                hi_mask |= static_cast<uint32_t>(b > bstar) << u;
+                eq_mask |= static_cast<uint32_t>(b == bstar) << u;
+            }
+        }
+        const uint32_t packed = (static_cast<uint32_t>(__popc(hi_mask)) << 16) | __popc(eq_mask);
+        uint32_t ptot;
+        const uint32_t pre = block_excl_scan(packed, c, ptot);
+        uint32_t hs = hi_base + (pre >> 16), es = eq_base + (pre & 0xFFFFu);
+#pragma unroll
+        for (int u = 0; u < GB; ++u) {
+            if ((hi_mask >> u) & 1u) sel[hs++] = v[u];
+            if ((eq_mask >> u) & 1u) blist[es++] = v[u];
+        }
+        hi_base += ptot >> 16;
+        eq_base += ptot & 0xFFFFu;
+    }
+    __syncthreads();
+    return rank_boundary<DT, NT>(blist, bsize, static_cast<uint32_t>(k) - above, above, det, sel, c);
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_constant__ Params p) {
     using raw_t = typename Elem<DT>::raw_t;
@@ -1296,8 +1480,6 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
 
     // chunk counts -> padded offsets (nch <= kFinalThreads, checked on the host)
     const uint32_t my = tid < nch ? __ldcg(row_counts(p, row) + tid) : 0u;
-#pragma unroll
-    for (int j = 0; j < kBins / kFinalThreads; ++j) hist[tid + j * kFinalThreads] = 0;
     const bool over = my > cap;
     const uint32_t cnt = over ? 0u : my;
     const uint32_t padded = (cnt + 1u) & ~1u;
@@ -1329,65 +1511,8 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
             if (tid < nch && (cnt & 1u)) cand[poff + cnt].y = kPadColumn;
             __syncthreads();
             GBTOPK_TRACE_POINT(1, 0);
-            for (uint32_t i = tid; i < total_p; i += kFinalThreads) {
-                const uint2 v = cand[i];
-                if (v.y != kPadColumn) atomicAdd(&hist[bin_of(Elem<DT>::key(v.x), t_lo, bin_shift)], 1u);
-            }
-            __syncthreads();
-            find_bin_from_top<kFinalThreads>(hist, static_cast<uint32_t>(k), c);
-            const uint32_t bstar = c.bcast[2], above = c.bcast[3], bsize = c.bcast[4];
-            if (bsize > static_cast<uint32_t>(kFinalBCap)) {
+            if (!select_gathered<DT, kFinalThreads>(cand, total_p, t_lo, bin_shift, k, det, hist, sel, blist, c))
                 fallback = true;
-            } else {
-                if (tid == 0) {
-                    c.sel_count = 0;
-                    c.b_count = 0;
-                }
-                __syncthreads();
-                // bins above b* go to sel, bin b* to blist (sel aliases the consumed histogram)
-                for (uint32_t i0 = 0; i0 < total_p; i0 += kFinalThreads) {
-                    const uint32_t i = i0 + tid;
-                    uint2 v = make_uint2(0, kPadColumn);
-                    if (i < total_p) v = cand[i];
-                    const bool live = v.y != kPadColumn;
-                    const uint32_t b = bin_of(Elem<DT>::key(v.x), t_lo, bin_shift);
-                    const bool hi = live && b > bstar, eq = live && b == bstar;
-                    const uint32_t hs = warp_claim(&c.sel_count, hi);
-                    if (hi) sel[hs] = v;
-                    const uint32_t es = warp_claim(&c.b_count, eq);
-                    if (eq) blist[es] = v;
-                }
-                __syncthreads();
-                GBTOPK_TRACE_POINT(3, 0);
-                const uint32_t need = static_cast<uint32_t>(k) - above;
-                if (bsize <= kRankMax) {
-                    for (uint32_t i = tid; i < bsize; i += kFinalThreads) {
-                        const uint2 me = blist[i];
-                        const uint32_t mk = Elem<DT>::key(me.x);
-                        uint32_t rank = 0;
-                        for (uint32_t j2 = 0; j2 < bsize; ++j2) {
-                            const uint2 o = blist[j2];
-                            const uint32_t ok = Elem<DT>::key(o.x);
-                            rank += (ok > mk || (ok == mk && o.y < me.y)) ? 1u : 0u;
-                        }
-                        if (rank < need) sel[above + rank] = me;
-                    }
-                    __syncthreads();
-                } else {
-                    constexpr int KB = Elem<DT>::kKeyBits;
-                    const PairSrc<DT> bs{blist};
-                    uint32_t t, gt;
-                    block_select<KB, KB / 8>(bs, RankByKey{}, bsize, need, c.rhist, c, t, gt);
-                    const uint32_t need_ties = need - gt;
-                    uint32_t col_max = 0xFFFFFFFFu;
-                    if (det) {
-                        uint32_t kk, g2;
-                        block_select<32, 4>(bs, RankTieColumn{t}, bsize, need_ties, c.rhist, c, kk, g2);
-                        col_max = ~kk;
-                    }
-                    collect<DT>(bs, bsize, t, gt, need_ties, det, col_max, sel, above, c);
-                }
-            }
         } else {
             fallback = true;
         }
@@ -1396,92 +1521,9 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
         const uint32_t base = block_excl_scan(cnt, c, total_p);
         if (tid < nch) choff[tid] = base;
         __syncthreads();
-        const SegMap map{segs, choff, static_cast<int>(nch), cap};
-        int cur = 0;
-        for (uint32_t b0 = 0; b0 < total; b0 += GB * kFinalThreads) {
-            const uint2 *addr[GB];
-            uint32_t raw[GB];
-#pragma unroll
-            for (int u = 0; u < GB; ++u) {
-                const uint32_t j = b0 + u * kFinalThreads + tid;
-                addr[u] = j < total ? map.at(j, cur) : nullptr;
-            }
-#pragma unroll
-            for (int u = 0; u < GB; ++u) raw[u] = addr[u] ? __ldcg(addr[u]).x : 0u;
-#pragma unroll
-            for (int u = 0; u < GB; ++u)
-                if (addr[u]) atomicAdd(&hist[bin_of(Elem<DT>::key(raw[u]), t_lo, bin_shift)], 1u);
-        }
-        __syncthreads();
-        find_bin_from_top<kFinalThreads>(hist, static_cast<uint32_t>(k), c);
-        const uint32_t bstar = c.bcast[2], above = c.bcast[3], bsize = c.bcast[4];
-        if (bsize > static_cast<uint32_t>(kFinalBCap)) {
+        if (!select_from_segments<DT, kFinalThreads>(SegMap{segs, choff, static_cast<int>(nch), cap}, total, t_lo,
+                                                     bin_shift, k, det, hist, sel, blist, c))
             fallback = true;
-        } else {
-            // bins above b* go to sel, bin b* to blist (count-then-write per batch)
-            uint32_t hi_base = 0, eq_base = 0;
-            int cur2 = 0;
-            for (uint32_t b0 = 0; b0 < total; b0 += GB * kFinalThreads) {
-                const uint2 *addr[GB];
-                uint2 v[GB];
-                uint32_t hi_mask = 0, eq_mask = 0;
-#pragma unroll
-                for (int u = 0; u < GB; ++u) {
-                    const uint32_t j = b0 + u * kFinalThreads + tid;
-                    addr[u] = j < total ? map.at(j, cur2) : nullptr;
-                }
-#pragma unroll
-                for (int u = 0; u < GB; ++u) v[u] = addr[u] ? __ldcg(addr[u]) : make_uint2(0, 0);
-#pragma unroll
-                for (int u = 0; u < GB; ++u) {
-                    if (addr[u]) {
-                        const uint32_t b = bin_of(Elem<DT>::key(v[u].x), t_lo, bin_shift);
-                        hi_mask |= static_cast<uint32_t>(b > bstar) << u;
-                        eq_mask |= static_cast<uint32_t>(b == bstar) << u;
-                    }
-                }
-                const uint32_t packed = (static_cast<uint32_t>(__popc(hi_mask)) << 16) | __popc(eq_mask);
-                uint32_t ptot;
-                const uint32_t pre = block_excl_scan(packed, c, ptot);
-                uint32_t hs = hi_base + (pre >> 16), es = eq_base + (pre & 0xFFFFu);
-#pragma unroll
-                for (int u = 0; u < GB; ++u) {
-                    if ((hi_mask >> u) & 1u) sel[hs++] = v[u];
-                    if ((eq_mask >> u) & 1u) blist[es++] = v[u];
-                }
-                hi_base += ptot >> 16;
-                eq_base += ptot & 0xFFFFu;
-            }
-            __syncthreads();
-            const uint32_t need = static_cast<uint32_t>(k) - above;
-            if (bsize <= kRankMax) {
-                for (uint32_t i = tid; i < bsize; i += kFinalThreads) {
-                    const uint2 me = blist[i];
-                    const uint32_t mk = Elem<DT>::key(me.x);
-                    uint32_t rank = 0;
-                    for (uint32_t j2 = 0; j2 < bsize; ++j2) {
-                        const uint2 o = blist[j2];
-                        const uint32_t ok = Elem<DT>::key(o.x);
-                        rank += (ok > mk || (ok == mk && o.y < me.y)) ? 1u : 0u;
-                    }
-                    if (rank < need) sel[above + rank] = me;
-                }
-                __syncthreads();
-            } else {
-                constexpr int KB = Elem<DT>::kKeyBits;
-                const PairSrc<DT> bs{blist};
-                uint32_t t, gt;
-                block_select<KB, KB / 8>(bs, RankByKey{}, bsize, need, c.rhist, c, t, gt);
-                const uint32_t need_ties = need - gt;
-                uint32_t col_max = 0xFFFFFFFFu;
-                if (det) {
-                    uint32_t kk, g2;
-                    block_select<32, 4>(bs, RankTieColumn{t}, bsize, need_ties, c.rhist, c, kk, g2);
-                    col_max = ~kk;
-                }
-                collect<DT>(bs, bsize, t, gt, need_ties, det, col_max, sel, above, c);
-            }
-        }
     }
     if (fallback) exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, det, sel, c.rhist, c);
     GBTOPK_TRACE_POINT(2, 0);
