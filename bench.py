@@ -35,10 +35,13 @@ METRIC = "top-K rows/s and HBM GB/s (% of GB300 peak), k=2048, N=163840/262144 f
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
 
-# DRAM bytes per launch from an ncu capture of the kernel (dram__bytes_read.sum
-# + dram__bytes_write.sum), keyed by the SHA-256 of the kernel source it was
-# taken on; reported as null once the kernel source changes.
-NCU_TRAFFIC = {}
+# DRAM bytes per call from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum summed over the call's kernels, cold cache), keyed by
+# workload and the SHA-256 prefix of the kernel source it was taken on;
+# reported as null once the kernel source changes.
+NCU_TRAFFIC = {
+    ("dsv32_decode", "36750825cd3e309e"): 23_982_176,
+}
 
 
 def parse():
@@ -333,7 +336,7 @@ def run_gbtopk(args, rank, world, local):
     avg_launch_s = statistics.mean(launch_ms) / 1e3
     peak, peak_src = peak_hbm()
     achieved = algo_bytes / avg_launch_s / 1e9
-    traffic = NCU_TRAFFIC.get(kernel_sha())
+    traffic = NCU_TRAFFIC.get((args.workload, kernel_sha()))
     plan = gb.gbtopk_plan_query(R, W, k, torch.float32)
     kernels_per_call = 3 if plan["split"] else 1
 
