@@ -1188,10 +1188,10 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
                 w[j] = v < nvec ? svec[v] : make_uint4(0, 0, 0, 0);
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&c.empty[s]);  // release: this warp's reads are done
         if (!ok) {
+            __syncwarp();
             if (lane == 0) {
+                mbar_arrive(&c.empty[s]);
                 atomicOr(reinterpret_cast<uint32_t *>(p.ws), kStatusWaitTimeout);
                 row_counts(p, grow)[m.chunk] = 0xFFFFFFFFu;  // finalize recomputes the row
             }
@@ -1229,17 +1229,30 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
         const uint32_t cap = static_cast<uint32_t>(m.seg_cap);
         uint2 *seg = row_segs(p, grow) + static_cast<int64_t>(m.chunk) * m.seg_cap;
         const int colbase = static_cast<int>(m.c0) - m.off;
+        // the lane's pass bits in one mask (bit EPV * j + q), then one
+        // iteration per candidate: its value is read back from the stage,
+        // which this warp releases only afterwards
+        constexpr int NW = (VPL * EPV + 31) / 32;
+        uint32_t mw[NW];
 #pragma unroll
-        for (int j = 0; j < VPL; ++j) {
-            uint32_t bits = msk[j];
-            const int vcol = colbase + (vbase + j * kGroupWarps * 32) * EPV;
+        for (int wd = 0; wd < NW; ++wd) mw[wd] = 0;
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) mw[(j * EPV) / 32] |= msk[j] << ((j * EPV) % 32);
+        const raw_t *selem = reinterpret_cast<const raw_t *>(svec);
+#pragma unroll
+        for (int wd = 0; wd < NW; ++wd) {
+            uint32_t bits = mw[wd];
             while (bits) {
-                const int q = __ffs(bits) - 1;
+                const int e = wd * 32 + __ffs(bits) - 1;
                 bits &= bits - 1;
-                if (slot < cap) seg[slot] = make_uint2(vec_elem<es>(w[j], q), static_cast<uint32_t>(vcol + q));
+                const int epos = (vbase + (e / EPV) * kGroupWarps * 32) * EPV + (e % EPV);
+                if (slot < cap) seg[slot] = make_uint2(static_cast<uint32_t>(selem[epos]),
+                                                       static_cast<uint32_t>(colbase + epos));
                 ++slot;
             }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.empty[s]);  // release: this warp's reads of the stage are done
     }
 #ifdef GBTOPK_TRACE
     t_busy += clock64() - t_mark;
