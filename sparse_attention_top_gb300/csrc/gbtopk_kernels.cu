@@ -30,6 +30,8 @@
 // denormals exact), so no float compare depends on flush-to-zero.
 #include <cstdint>
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "gbtopk_internal.h"
@@ -591,14 +593,54 @@ __device__ __forceinline__ float float_of_key(uint32_t t) {
 // Threshold test of one raw element: key(raw) >= t_lo.  For fp32 it is one
 // float compare against the float whose key is t_lo (signed zeros compare
 // equal in IEEE arithmetic, so the two tests agree).
+//
+// mask(w) tests the 16-byte vector w at once (bit q = element q).  For the
+// 16-bit types it compares packed pairs against the raw value whose key is
+// t_lo: IEEE order, with signed zeros equal, is the key order.  A compare
+// that flushed subnormals to zero could only turn "below" into "equal"
+// (flushing is monotone), so it can add candidates but never drop one.
 template <int DT>
 struct PassTest {
     uint32_t t_lo;
     float tf;
-    __device__ __forceinline__ explicit PassTest(uint32_t t) : t_lo(t), tf(float_of_key(t)) {}
+    uint32_t t2;  // 16-bit types: the threshold's raw value in both halves
+    __device__ __forceinline__ explicit PassTest(uint32_t t) : t_lo(t), tf(float_of_key(t)) {
+        const uint32_t r16 = (t & 0x8000u) ? (t & 0x7FFFu) : (~t & 0xFFFFu);
+        t2 = r16 | (r16 << 16);
+    }
     __device__ __forceinline__ bool operator()(uint32_t raw) const {
         if (Elem<DT>::kBytes == 4) return __uint_as_float(raw) >= tf;
         return Elem<DT>::key(raw) >= t_lo;
+    }
+    __device__ __forceinline__ static uint32_t pair_bits(uint32_t m) {  // 0xFFFF halves -> 2 bits
+        return (m & 1u) | ((m >> 15) & 2u);
+    }
+    __device__ __forceinline__ uint32_t pair_mask(uint32_t word) const {
+        if constexpr (DT == 1) {
+            __nv_bfloat162_raw a, b;
+            a.x = static_cast<unsigned short>(word & 0xFFFFu);
+            a.y = static_cast<unsigned short>(word >> 16);
+            b.x = static_cast<unsigned short>(t2 & 0xFFFFu);
+            b.y = static_cast<unsigned short>(t2 >> 16);
+            return pair_bits(__hge2_mask(__nv_bfloat162(a), __nv_bfloat162(b)));
+        } else {
+            __half2_raw a, b;
+            a.x = static_cast<unsigned short>(word & 0xFFFFu);
+            a.y = static_cast<unsigned short>(word >> 16);
+            b.x = static_cast<unsigned short>(t2 & 0xFFFFu);
+            b.y = static_cast<unsigned short>(t2 >> 16);
+            return pair_bits(__hge2_mask(__half2(a), __half2(b)));
+        }
+    }
+    __device__ __forceinline__ uint32_t mask(const uint4 &w) const {
+        if constexpr (Elem<DT>::kBytes == 4) {
+            return static_cast<uint32_t>(__uint_as_float(w.x) >= tf) |
+                   (static_cast<uint32_t>(__uint_as_float(w.y) >= tf) << 1) |
+                   (static_cast<uint32_t>(__uint_as_float(w.z) >= tf) << 2) |
+                   (static_cast<uint32_t>(__uint_as_float(w.w) >= tf) << 3);
+        } else {
+            return pair_mask(w.x) | (pair_mask(w.y) << 2) | (pair_mask(w.z) << 4) | (pair_mask(w.w) << 6);
+        }
     }
 };
 
@@ -737,10 +779,7 @@ __device__ uint32_t filter_staged(const void *stage, int off, int len, int col_b
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         const int v = threadIdx.x + j * static_cast<int>(blockDim.x);
-        uint32_t m = 0;
-#pragma unroll
-        for (int q = 0; q < EPV; ++q) m |= static_cast<uint32_t>(pass(vec_elem<es>(w[j], q))) << q;
-        msk[j] = m & valid_lanes<EPV>(v, nvec, off, len);
+        msk[j] = pass.mask(w[j]) & valid_lanes<EPV>(v, nvec, off, len);
         cnt += __popc(msk[j]);
     }
     uint32_t total;
@@ -1203,9 +1242,7 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
 #pragma unroll
         for (int j = 0; j < VPL; ++j) {
             const int v = vbase + j * kGroupWarps * 32;
-            uint32_t bits = 0;
-#pragma unroll
-            for (int q = 0; q < EPV; ++q) bits |= static_cast<uint32_t>(pass(vec_elem<es>(w[j], q))) << q;
+            uint32_t bits = pass.mask(w[j]);
             if (v == 0 || v >= nvec - 1) bits &= valid_lanes<EPV>(v, nvec, m.off, m.len);
             msk[j] = bits;
             cnt += __popc(bits);
