@@ -1585,6 +1585,137 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
                               (static_cast<unsigned long long>(total) << 40));
 }
 
+// ---------------------------------------------------------------- small rows
+
+// Small-row kernel (widths up to 32 * NE <= 2048 columns, non-deterministic
+// calls): one warp per row, no block barrier.  Lane l holds columns l,
+// l + 32, ..., as keys in registers.  The k-th largest key t comes from a
+// radix select over 8-bit digits with a warp-private 256-bin shared
+// histogram (two rounds for 16-bit keys, four for fp32).  The keys above t
+// and the first k - #(keys > t) keys equal to t in column order are then
+// written in column order, each warp-wide slot from two ballots per
+// register.
+template <int DT, int NE>
+__global__ void __launch_bounds__(128) small_kernel(const __grid_constant__ Params p) {
+    using raw_t = typename Elem<DT>::raw_t;
+    constexpr int KB = Elem<DT>::kKeyBits;
+    const uint32_t lane = lane_id();
+    __shared__ uint32_t small_hist[4 * 256];  // one digit histogram per warp
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+    if (row >= p.num_rows) return;  // whole warps
+    const int k = p.k;
+    int64_t n, col0;
+    row_window(p, row, n, col0);
+    const raw_t *xrow = static_cast<const raw_t *>(p.x) + row * p.row_stride + col0;
+    int32_t *out = p.out_idx + row * k;
+    // the unrolled selection below stores bare column indices in out; a
+    // rolled pass then applies the page-table transform and the values
+    if (n <= k) {  // short and empty rows: every valid column in order, then -1
+        for (int64_t j = lane; j < k; j += 32) out[j] = j < n ? static_cast<int32_t>(j) : -1;
+    } else {
+        uint32_t key[NE];
+#pragma unroll
+        for (int e = 0; e < NE; ++e) {
+            const int64_t c = lane + 32 * e;
+            key[e] = c < n ? Elem<DT>::key(ldg_raw(xrow + c)) : 0u;
+        }
+        // the k-th largest key: radix select over 8-bit digits from the top,
+        // one 256-bin shared histogram per warp (columns past the row hold
+        // key 0, which no real value maps to, and are left out)
+        uint32_t *h = small_hist + (threadIdx.x >> 5) * 256;
+        uint32_t prefix = 0, pmask = 0, rem = static_cast<uint32_t>(k);
+#pragma unroll 1
+        for (int shift = KB - 8; shift >= 0; shift -= 8) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) h[lane + 32 * i] = 0;
+            __syncwarp();
+#pragma unroll
+            for (int e = 0; e < NE; ++e)
+                if (key[e] != 0u && (key[e] & pmask) == prefix) atomicAdd(&h[(key[e] >> shift) & 255u], 1u);
+            __syncwarp();
+            uint32_t cnt[8], sum = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                cnt[j] = h[255 - 8 * lane - j];
+                sum += cnt[j];
+            }
+            uint32_t incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= static_cast<uint32_t>(o)) incl += y;
+            }
+            const uint32_t excl = incl - sum;
+            const uint32_t owner = __ffs(__ballot_sync(0xffffffffu, excl < rem && rem <= incl)) - 1;
+            uint32_t digit = 0, above = excl;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (above + cnt[j] >= rem) {
+                    digit = 255u - 8u * lane - static_cast<uint32_t>(j);
+                    break;
+                }
+                above += cnt[j];
+            }
+            digit = __shfl_sync(0xffffffffu, digit, owner);
+            above = __shfl_sync(0xffffffffu, above, owner);
+            prefix |= digit << shift;
+            pmask |= 255u << shift;
+            rem -= above;
+            __syncwarp();
+        }
+        const uint32_t t = prefix;
+        const uint32_t gt = static_cast<uint32_t>(k) - rem;
+        const uint32_t need = rem;  // ties taken, smallest columns first
+        const uint32_t lt = lanemask_lt();
+        uint32_t hi_base = 0, tie_base = 0;
+#pragma unroll
+        for (int e = 0; e < NE; ++e) {
+            const bool h = key[e] > t, q = key[e] == t;
+            const uint32_t bh = __ballot_sync(0xffffffffu, h);
+            const uint32_t bt = __ballot_sync(0xffffffffu, q);
+            const uint32_t r = tie_base + __popc(bt & lt);
+            const uint32_t slot = h ? hi_base + __popc(bh & lt) : gt + r;
+            if (h || (q && r < need)) out[slot] = static_cast<int32_t>(lane + 32 * e);
+            hi_base += __popc(bh);
+            tie_base += __popc(bt);
+        }
+    }
+    if (!p.page_table && !p.out_val) return;
+    __syncwarp();  // the warp's index stores are visible to its lanes
+    int64_t pt_start = 0;
+    if (p.page_table) {
+        if (p.pt_row_starts) pt_start = __ldg(p.pt_row_starts + row);
+        else if (p.pt_start_is_row_start) pt_start = __ldg(p.row_starts + row);
+    }
+#pragma unroll 1
+    for (int64_t j = lane; j < k; j += 32) {
+        const int32_t idx = out[j];
+        if (p.out_val)
+            static_cast<raw_t *>(p.out_val)[row * k + j] =
+                static_cast<raw_t>(idx >= 0 ? ldg_raw(xrow + idx) : Elem<DT>::kLowest);
+        if (p.page_table) {
+            int32_t v = -1;
+            if (idx >= 0) {
+                const int64_t col = pt_start + idx / p.page_size;
+                if (col >= 0 && col < p.pt_cols) {
+                    const int64_t page = __ldg(p.page_table + row * p.pt_row_stride + col);
+                    v = static_cast<int32_t>(static_cast<uint32_t>(
+                        static_cast<uint64_t>(page * p.page_size + idx % p.page_size)));
+                }
+            }
+            if (p.out_raw) p.out_raw[row * k + j] = idx;
+            out[j] = v;
+        }
+    }
+}
+
+template <int DT, int NE>
+cudaError_t launch_small(const Params &p, cudaStream_t stream) {
+    const unsigned grid = static_cast<unsigned>((p.num_rows + 3) / 4);
+    small_kernel<DT, NE><<<grid, 128, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
 template <class K>
 cudaError_t set_smem(K kern, size_t bytes, size_t &configured) {
     if (bytes > 48 * 1024 && bytes > configured) {
@@ -1623,6 +1754,11 @@ cudaError_t launch_dt(const Params &p0, cudaStream_t stream) {
         Params p = p0;
         p.row0 = 0;
         p.rows = p0.num_rows;
+        if (!p.deterministic && p.width <= 32 * 64) {  // one warp per row
+            if (p.width <= 32 * 16) return launch_small<DT, 16>(p, stream);
+            if (p.width <= 32 * 32) return launch_small<DT, 32>(p, stream);
+            return launch_small<DT, 64>(p, stream);
+        }
         return launch_row_any<DT>(p, stream);
     }
     if ((e = set_smem(stream_kernel<DT>, p0.plan.stream_smem, cfg_stream)) != cudaSuccess) return e;

@@ -166,6 +166,35 @@ def test_ties_and_specials(dev, dtype, W, det):
         run_case(dev, c, det=det)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("W", [33, 512, 1000, 2048])
+def test_small_rows_warp_path(dev, dtype, W):
+    """Widths up to 2048 without the deterministic order take the one-warp-per-row
+    path: ragged lengths (empty, 1, around k, full, beyond the width), ties, signed
+    zeros and infinities, every k from 1 to 2048, values on."""
+    g = torch.Generator().manual_seed(W + 7)
+    R = 40
+    x = torch.randn(R, W, generator=g)
+    x[1::4] = torch.round(x[1::4] * 2) / 2                        # heavy ties
+    x[2, ::3] = -0.0
+    x[2, 1::3] = 0.0
+    x[3, ::5] = float("inf")
+    x[3, 1::7] = float("-inf")
+    x[5] = 0.25                                                    # all equal
+    for k in (1, 7, 64, 512, 2048):
+        lens = torch.randint(0, W + 40, (R,), generator=g, dtype=torch.int32)
+        lens[0], lens[4], lens[6] = 0, 1, W
+        lens[7], lens[8] = min(k, W), min(k + 1, W)
+        c = workloads.VarlenCase("small", x.to(dtype), lens, k)
+        run_case(dev, c)
+
+
+def test_small_rows_page_table(dev):
+    c = workloads.page_table_case(rows=48, width=1500, row_stride=1531, page_size=16,
+                                  pt_cols=128, top_k=256, deterministic=False, seed=5077)
+    _run_page_table(dev, c)
+
+
 def test_misaligned_and_strided_views(dev):
     c = workloads.dsv32_decode(rows=6, width=30001, top_k=1024, hinted=False, seed=2050)
 
