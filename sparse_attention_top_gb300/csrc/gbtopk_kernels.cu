@@ -926,10 +926,29 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
         if (threadIdx.x == kHintThread && p.pre_idx) a = __ldg(p.pre_idx + (row / p.next_n) * k);
         if (n > kSampleSize) {
             m = kSampleSize;
-            const int64_t pos = static_cast<int64_t>(threadIdx.x) * (n - 8) / (kSampleGroups - 1);
+            // group of 8 consecutive columns, moved down to a 16-byte
+            // boundary (one or two vector loads) unless that would leave the row
+            int64_t pos = static_cast<int64_t>(threadIdx.x) * (n - 8) / (kSampleGroups - 1);
+            const uintptr_t addr = reinterpret_cast<uintptr_t>(xrow + pos);
+            const int64_t back = static_cast<int64_t>((addr & 15u) / Elem<DT>::kBytes);
             uint32_t raw[8];
+            if (back <= pos) {
+                pos -= back;
+                const uint4 *v = reinterpret_cast<const uint4 *>(xrow + pos);
+                if constexpr (Elem<DT>::kBytes == 4) {
+                    const uint4 a = __ldg(v), b = __ldg(v + 1);
+                    raw[0] = a.x; raw[1] = a.y; raw[2] = a.z; raw[3] = a.w;
+                    raw[4] = b.x; raw[5] = b.y; raw[6] = b.z; raw[7] = b.w;
+                } else {
+                    const uint4 a = __ldg(v);
+                    const uint32_t wd[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-            for (int j = 0; j < 8; ++j) raw[j] = ldg_raw(xrow + pos + j);
+                    for (int j = 0; j < 8; ++j) raw[j] = (wd[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) raw[j] = ldg_raw(xrow + pos + j);
+            }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const uint32_t key = Elem<DT>::key(raw[j]);
