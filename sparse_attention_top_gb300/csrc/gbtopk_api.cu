@@ -62,7 +62,9 @@ int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *p
         if (pl.chunks_per_row > kFinalThreads) return GBTOPK_EUNSUPPORTED;
         hist = hist > big_hist ? hist : big_hist;
         pl.block_rows = num_rows < kMaxBlockRows ? num_rows : kMaxBlockRows;
-        pl.stream_smem = kCtrlBytes + align_up(static_cast<size_t>(kMaxBlockRows + 1) * 16, 128) +
+        // control block, the row table of one launch, the ring (a small
+        // batch's stream block still fits beside a row-kernel block)
+        pl.stream_smem = kCtrlBytes + align_up(static_cast<size_t>(pl.block_rows + 1) * 16, 128) +
                          static_cast<size_t>(kStages) * kStageBytes;
         // finalize: control, histogram / selection, boundary bin, chunk
         // offsets, then the gathered candidates (kGatherCandidates)

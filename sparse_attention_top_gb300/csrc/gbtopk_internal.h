@@ -19,7 +19,7 @@ constexpr int kBins = 1 << kBinBits;   // candidate histogram bins
 constexpr int kRankMax = 256;          // boundary-bin size resolved by rank counting
 constexpr size_t kCtrlBytes = 2048;    // per-block control block (counters, scan, digit histogram)
 constexpr int kChunkBytes = 32768;     // bytes per stream chunk (one bulk copy)
-constexpr int kStages = 4;             // bulk-copy ring depth of the stream kernel
+constexpr int kStages = 6;             // bulk-copy ring depth of the stream kernel
 constexpr int kGroupWarps = 8;         // consumer warps that share one chunk
 constexpr int kStageBytes = kChunkBytes + 32;  // a chunk plus its 16-byte alignment slack
 constexpr int kStreamThreads = 544;    // stream kernel: 1 producer warp + 16 consumer warps
