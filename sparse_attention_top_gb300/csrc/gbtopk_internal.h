@@ -27,6 +27,7 @@ constexpr int kFinalHistBytes = 16384; // finalize histogram / selection buffer
 constexpr int kMaxBlockRows = 2048;    // rows per launch of the split pipeline
 constexpr int kFinalBCap = 2048;       // boundary-bin members the finalize kernel can hold
 constexpr int kGatherCandidates = 8192; // candidates the finalize kernel gathers into shared memory
+constexpr size_t kDetScratchBytes = (1u << 12) * 4 + 2048 * 8;  // deterministic output: bin counters + pairs
 constexpr size_t kWsHeaderBytes = 256; // device status word + padding
 constexpr size_t kRowInfoBytes = 16;   // t_lo, bin shift (written by the row kernel)
 constexpr uint32_t kSpinLimit = 1u << 22;

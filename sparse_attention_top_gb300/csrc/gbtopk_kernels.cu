@@ -199,6 +199,18 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, Ctrl &c, uint32_
     return r;
 }
 
+// Block-wide min and max of one key per thread into c.key_min / c.key_max
+// (which thread 0 must have reset to ~0u / 0 before a preceding barrier).
+__device__ __forceinline__ void block_minmax(uint32_t kmin, uint32_t kmax, Ctrl &c) {
+    kmin = __reduce_min_sync(0xffffffffu, kmin);
+    kmax = __reduce_max_sync(0xffffffffu, kmax);
+    if (lane_id() == 0) {
+        atomicMin(&c.key_min, kmin);
+        atomicMax(&c.key_max, kmax);
+    }
+    __syncthreads();
+}
+
 // ---------------------------------------------------------------- bulk copy (TMA)
 
 __device__ __forceinline__ void mbar_init(unsigned long long *bar) {
@@ -443,36 +455,6 @@ __device__ void exact_select(const S &s, int64_t n, int k, bool det, uint2 *sel,
     collect<DT>(s, n, t, gt, need_ties, det, col_max, sel, 0, c);
 }
 
-// Orders sel[0..m) by (key desc, column asc) with a bitonic network over the
-// next power of two; the padding sorts last.
-template <int DT>
-__device__ void sort_selection(uint2 *sel, int m) {
-    int p2 = 1;
-    while (p2 < m) p2 <<= 1;
-    for (int i = m + threadIdx.x; i < p2; i += blockDim.x)
-        sel[i] = make_uint2(Elem<DT>::kKeyZeroRaw, 0x7FFFFFFFu);
-    __syncthreads();
-    auto comp = [](uint2 v) -> unsigned long long {
-        return (static_cast<unsigned long long>(Elem<DT>::key(v.x)) << 32) |
-               static_cast<unsigned long long>(0xFFFFFFFFu - v.y);
-    };
-    for (int size = 2; size <= p2; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = threadIdx.x; i < (p2 >> 1); i += blockDim.x) {
-                const int lo = 2 * i - (i & (stride - 1));
-                const int hi = lo + stride;
-                const bool desc = (lo & size) == 0;
-                const uint2 a = sel[lo], b = sel[hi];
-                if ((comp(a) < comp(b)) == desc) {
-                    sel[lo] = b;
-                    sel[hi] = a;
-                }
-            }
-            __syncthreads();
-        }
-    }
-}
-
 // ---------------------------------------------------------------- row geometry and output
 
 __device__ __forceinline__ void row_window(const Params &p, int64_t row, int64_t &n, int64_t &col0) {
@@ -495,38 +477,121 @@ __device__ __forceinline__ void row_window(const Params &p, int64_t row, int64_t
     }
 }
 
+// One output slot j of `row`: the index (page-table transformed when a
+// table is given, the raw index then going to out_raw) and the value
+// (bit copy, or the dtype's lowest finite value for a -1 slot).
 template <int DT>
-__device__ void emit(const Params &p, int64_t row, const uint2 *sel, int m) {
+__device__ __forceinline__ void put_slot(const Params &p, int64_t row, int64_t pt_start, int j, int32_t idx,
+                                         uint32_t raw) {
     using raw_t = typename Elem<DT>::raw_t;
     const int k = p.k;
-    int64_t pt_start = 0;
-    if (p.page_table) {
-        if (p.pt_row_starts) pt_start = __ldg(p.pt_row_starts + row);
-        else if (p.pt_start_is_row_start) pt_start = __ldg(p.row_starts + row);
-    }
     int32_t *out = p.out_idx + row * k;
-    for (int j = threadIdx.x; j < k; j += blockDim.x) {
-        const bool live = j < m;
-        const int32_t idx = live ? static_cast<int32_t>(sel[j].y) : -1;
-        if (p.page_table) {
-            int32_t v = -1;
-            if (idx >= 0) {
-                const int64_t col = pt_start + idx / p.page_size;
-                if (col >= 0 && col < p.pt_cols) {
-                    const int64_t page = __ldg(p.page_table + row * p.pt_row_stride + col);
-                    v = static_cast<int32_t>(static_cast<uint32_t>(
-                        static_cast<uint64_t>(page * p.page_size + idx % p.page_size)));
-                }
+    if (p.page_table) {
+        int32_t v = -1;
+        if (idx >= 0) {
+            const int64_t col = pt_start + idx / p.page_size;
+            if (col >= 0 && col < p.pt_cols) {
+                const int64_t page = __ldg(p.page_table + row * p.pt_row_stride + col);
+                v = static_cast<int32_t>(static_cast<uint32_t>(
+                    static_cast<uint64_t>(page * p.page_size + idx % p.page_size)));
             }
-            out[j] = v;
-            if (p.out_raw) p.out_raw[row * k + j] = idx;
-        } else {
-            out[j] = idx;
         }
-        if (p.out_val)
-            static_cast<raw_t *>(p.out_val)[row * k + j] =
-                static_cast<raw_t>(live ? sel[j].x : Elem<DT>::kLowest);
+        out[j] = v;
+        if (p.out_raw) p.out_raw[row * k + j] = idx;
+    } else {
+        out[j] = idx;
     }
+    if (p.out_val)
+        static_cast<raw_t *>(p.out_val)[row * k + j] = static_cast<raw_t>(idx >= 0 ? raw : Elem<DT>::kLowest);
+}
+
+__device__ __forceinline__ int64_t page_table_start(const Params &p, int64_t row) {
+    if (!p.page_table) return 0;
+    if (p.pt_row_starts) return __ldg(p.pt_row_starts + row);
+    if (p.pt_start_is_row_start) return __ldg(p.row_starts + row);
+    return 0;
+}
+
+template <int DT>
+__device__ void emit(const Params &p, int64_t row, const uint2 *sel, int m) {
+    const int64_t pt_start = page_table_start(p, row);
+    for (int j = threadIdx.x; j < p.k; j += blockDim.x) {
+        const bool live = j < m;
+        put_slot<DT>(p, row, pt_start, j, live ? static_cast<int32_t>(sel[j].y) : -1, live ? sel[j].x : 0u);
+    }
+}
+
+// Deterministic output (value desc, column asc) of the m selected pairs in
+// sel, written straight to their output slots.  The keys are counted in
+// kBins bins over their own range; an exclusive scan from the top gives
+// each bin's first slot, the pairs are scattered into their bins' segments
+// (scratch), and each pair's slot is its segment's start plus the number of
+// segment mates that order before it.  Slots m .. k-1 get -1.  `scratch`
+// holds kBins counters and m pairs (kDetScratchBytes).  All threads call it.
+template <int DT>
+__device__ void emit_sorted(const Params &p, int64_t row, const uint2 *sel, int m, uint8_t *scratch, Ctrl &c) {
+    uint32_t *bins = reinterpret_cast<uint32_t *>(scratch);
+    uint2 *seg = reinterpret_cast<uint2 *>(scratch + kBins * 4);
+    const int nt = blockDim.x;
+    const int tid = threadIdx.x;
+    const int64_t pt_start = page_table_start(p, row);
+    if (tid == 0) {
+        c.key_min = 0xFFFFFFFFu;
+        c.key_max = 0;
+    }
+    for (int b = tid; b < kBins; b += nt) bins[b] = 0;
+    __syncthreads();
+    uint32_t kmin = 0xFFFFFFFFu, kmax = 0;
+    for (int i = tid; i < m; i += nt) {
+        const uint32_t key = Elem<DT>::key(sel[i].x);
+        kmin = key < kmin ? key : kmin;
+        kmax = key > kmax ? key : kmax;
+    }
+    block_minmax(kmin, kmax, c);
+    kmin = c.key_min;
+    const int bits = 32 - __clz(c.key_max - kmin);
+    const int shift = bits > kBinBits ? bits - kBinBits : 0;
+    for (int i = tid; i < m; i += nt)
+        atomicAdd(&bins[(Elem<DT>::key(sel[i].x) - kmin) >> shift], 1u);
+    __syncthreads();
+    // exclusive scan from the top: bins[b] = pairs in the bins above b
+    {
+        const int bpt = kBins / nt;  // bins per thread, from the top down
+        uint32_t sum = 0;
+        for (int j = 0; j < bpt; ++j) sum += bins[kBins - 1 - bpt * tid - j];
+        uint32_t tot;
+        uint32_t run = block_excl_scan(sum, c, tot);
+        for (int j = 0; j < bpt; ++j) {
+            const int b = kBins - 1 - bpt * tid - j;
+            const uint32_t cnt = bins[b];
+            bins[b] = run;
+            run += cnt;
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < m; i += nt) {
+        const uint2 v = sel[i];
+        seg[atomicAdd(&bins[(Elem<DT>::key(v.x) - kmin) >> shift], 1u)] = v;
+    }
+    __syncthreads();
+    // bins[b] now ends b's segment, which starts where b + 1's ends
+    for (int j = tid; j < m; j += nt) {
+        const uint2 v = seg[j];
+        const int b = static_cast<int>((Elem<DT>::key(v.x) - kmin) >> shift);
+        const uint32_t lo = b == kBins - 1 ? 0u : bins[b + 1], hi = bins[b];
+        const unsigned long long mine = (static_cast<unsigned long long>(Elem<DT>::key(v.x)) << 32) |
+                                        static_cast<unsigned long long>(0xFFFFFFFFu - v.y);
+        uint32_t before = 0;
+        for (uint32_t i = lo; i < hi; ++i) {
+            const uint2 o = seg[i];
+            const unsigned long long oc = (static_cast<unsigned long long>(Elem<DT>::key(o.x)) << 32) |
+                                          static_cast<unsigned long long>(0xFFFFFFFFu - o.y);
+            before += oc > mine ? 1u : 0u;
+        }
+        put_slot<DT>(p, row, pt_start, static_cast<int>(lo + before), static_cast<int32_t>(v.y), v.x);
+    }
+    for (int j = m + tid; j < p.k; j += nt) put_slot<DT>(p, row, pt_start, j, -1, 0u);
+    __syncthreads();
 }
 
 // ---------------------------------------------------------------- bulk staging
@@ -739,17 +804,6 @@ __device__ void guess_from_sample(const uint32_t *sample, int m, int64_t n, int 
     bin_shift = bits > kBinBits - 1 ? bits - (kBinBits - 1) : 0;
 }
 
-// Block-wide min and max of one key per thread into c.key_min / c.key_max
-// (which thread 0 must have reset to ~0u / 0 before a preceding barrier).
-__device__ __forceinline__ void block_minmax(uint32_t kmin, uint32_t kmax, Ctrl &c) {
-    kmin = __reduce_min_sync(0xffffffffu, kmin);
-    kmax = __reduce_max_sync(0xffffffffu, kmax);
-    if (lane_id() == 0) {
-        atomicMin(&c.key_min, kmin);
-        atomicMax(&c.key_max, kmax);
-    }
-    __syncthreads();
-}
 
 // ---------------------------------------------------------------- block filter
 
@@ -998,8 +1052,8 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
         for (int j = threadIdx.x; j < n; j += blockDim.x)
             sel[j] = make_uint2(need_raw ? ldg_raw(xrow + j) : 0u, static_cast<uint32_t>(j));
         __syncthreads();
-        if (det) sort_selection<DT>(sel, static_cast<int>(n));
-        emit<DT>(p, row, sel, static_cast<int>(n));
+        if (det) emit_sorted<DT>(p, row, sel, static_cast<int>(n), smem + p.plan.row_smem, c);
+        else emit<DT>(p, row, sel, static_cast<int>(n));
         GBTOPK_TRACE_POINT(6, 0);
         GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | 1u);
         return;
@@ -1048,8 +1102,8 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
                                                         k, det, sel, lcand + total, stage_pairs - total, c);
     }
     if (!done) exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, det, sel, c.rhist, c);
-    if (det) sort_selection<DT>(sel, k);
-    emit<DT>(p, row, sel, k);
+    if (det) emit_sorted<DT>(p, row, sel, k, smem + p.plan.row_smem, c);
+    else emit<DT>(p, row, sel, k);
     if (!ok && threadIdx.x == 0) mbar_wait(&c.bar, 0);  // let the copy land before exit
     GBTOPK_TRACE_POINT(6, 0);
     GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | 2u);
@@ -1596,9 +1650,13 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
     }
     if (fallback) exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, det, sel, c.rhist, c);
     GBTOPK_TRACE_POINT(2, 0);
-    if (det) sort_selection<DT>(sel, k);
-    emit<DT>(p, row, sel, k);
-    if (!copy_ok && tid == 0) mbar_wait(&c.bar, 0);  // let the copies land before exit
+    if (!copy_ok && tid == 0) mbar_wait(&c.bar, 0);  // let the copies land (before reusing cand)
+    if (det) {
+        __syncthreads();
+        emit_sorted<DT>(p, row, sel, k, reinterpret_cast<uint8_t *>(cand), c);
+    } else {
+        emit<DT>(p, row, sel, k);
+    }
     GBTOPK_TRACE_POINT(6, 0);
     GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | (fallback ? 5u : (in_smem ? 4u : 3u)) |
                               (static_cast<unsigned long long>(total) << 40));
@@ -1749,9 +1807,10 @@ cudaError_t set_smem(K kern, size_t bytes, size_t &configured) {
 template <int DT, int VPT>
 cudaError_t launch_row(const Params &p, cudaStream_t stream) {
     static size_t configured = 0;  // largest dynamic smem opted in so far
-    const cudaError_t e = set_smem(row_kernel<DT, VPT>, p.plan.row_smem, configured);
+    const size_t bytes = p.plan.row_smem + (p.deterministic ? kDetScratchBytes : 0);
+    const cudaError_t e = set_smem(row_kernel<DT, VPT>, bytes, configured);
     if (e != cudaSuccess) return e;
-    row_kernel<DT, VPT><<<static_cast<unsigned>(p.rows), kThreads, p.plan.row_smem, stream>>>(p);
+    row_kernel<DT, VPT><<<static_cast<unsigned>(p.rows), kThreads, bytes, stream>>>(p);
     return cudaGetLastError();
 }
 
