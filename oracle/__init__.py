@@ -58,6 +58,12 @@ def _load():
             lib.oracle_page_table_transform.argtypes = [
                 vp, ctypes.c_int, i64, i64, i64, vp, vp, vp, i64, i64, vp, i32, i32,
                 vp, vp]
+            lib.oracle_ragged_offset_transform.restype = ctypes.c_int
+            lib.oracle_ragged_offset_transform.argtypes = [
+                vp, ctypes.c_int, i64, i64, i64, vp, vp, vp, i32, vp]
+            lib.oracle_seqs_page_table_transform.restype = ctypes.c_int
+            lib.oracle_seqs_page_table_transform.argtypes = [
+                vp, ctypes.c_int, i64, i64, i64, vp, vp, vp, i64, i64, vp, i64, i32, vp]
             _lib = lib
     return _lib
 
@@ -148,3 +154,44 @@ def page_table_transform(scores, lengths, page_table, top_k: int, page_size: int
     if rc != 0:
         raise ValueError(f"oracle_page_table_transform failed: {rc}")
     return out, out_raw
+
+
+def ragged_offset_transform(scores, lengths, offsets, top_k: int, row_starts=None):
+    """Oracle of the ragged KV offset transform: out = idx + offsets[row]."""
+    import torch
+    assert scores.dim() == 2 and scores.stride(1) == 1
+    R, W = scores.shape
+    S = scores.stride(0) if R > 1 else W
+    ln = lengths.to(torch.int32).contiguous()
+    rs = row_starts.to(torch.int32).contiguous() if row_starts is not None else None
+    off = offsets.to(torch.int32).contiguous()
+    out = torch.empty((R, top_k), dtype=torch.int32)
+    rc = _load().oracle_ragged_offset_transform(
+        _ptr(scores), DTYPE_CODES[_dtype_name(scores)], R, W, S, _ptr(ln), _ptr(rs), _ptr(off),
+        top_k, _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_ragged_offset_transform failed: {rc}")
+    return out
+
+
+def seqs_page_table_transform(scores, lengths, page_table, cu_seqlens_q, top_k: int,
+                              row_starts=None):
+    """Oracle of the page_size-1 page-table transform over requests
+    (row r belongs to request b with cu_seqlens_q[b] <= r < cu_seqlens_q[b+1])."""
+    import torch
+    assert scores.dim() == 2 and scores.stride(1) == 1
+    assert page_table.dim() == 2 and page_table.stride(1) == 1
+    R, W = scores.shape
+    S = scores.stride(0) if R > 1 else W
+    ln = lengths.to(torch.int32).contiguous()
+    rs = row_starts.to(torch.int32).contiguous() if row_starts is not None else None
+    cu = cu_seqlens_q.to(torch.int32).contiguous()
+    P = page_table.shape[1]
+    PS = page_table.stride(0) if page_table.shape[0] > 1 else P
+    out = torch.empty((R, top_k), dtype=torch.int32)
+    rc = _load().oracle_seqs_page_table_transform(
+        _ptr(scores), DTYPE_CODES[_dtype_name(scores)], R, W, S, _ptr(ln), _ptr(rs),
+        _ptr(page_table), P, PS, _ptr(cu), cu.numel() - 1, top_k, _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_seqs_page_table_transform failed: {rc}")
+    return out

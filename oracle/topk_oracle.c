@@ -41,6 +41,16 @@
  *    clamped to the width; a row_start outside [0, width] gives an empty row;
  *  - a page-table column outside [0, pt_cols) yields -1 in `out`;
  *  - page * page_size + idx % page_size must fit in int32 (error otherwise).
+ *
+ * Two more epilogues of the same selection (SGLang TopK ops wiki,
+ * fast_topk_transform_ragged_fused and fast_topk_transform_fused):
+ *  - ragged KV offset: out = idx + topk_indices_offset[row], -1 stays -1;
+ *  - page table with page_size 1 over requests: row r belongs to request b
+ *    with cu_seqlens_q[b] <= r < cu_seqlens_q[b + 1], and
+ *    out = page_table[b, idx], -1 stays -1.
+ * Readings: idx is the row-local index in both (relative to row_start); a
+ * row no request covers is empty (all -1); an idx at or beyond pt_cols
+ * yields -1; idx + offset must fit in int32 (error otherwise).
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -252,6 +262,88 @@ int oracle_page_table_transform(const void *scores, int dtype, int64_t num_rows,
                 return OR_ERANGE;
             }
             out[r * k + s] = (int32_t)phys;
+        }
+    }
+    free(raw);
+    return OR_OK;
+}
+
+/* Ragged KV offset transform (SGLang TopK ops, fast_topk_transform_ragged_fused):
+ * each selected row-local index idx becomes idx + offsets[row]; -1 stays -1. */
+int oracle_ragged_offset_transform(const void *scores, int dtype, int64_t num_rows,
+                                   int64_t width, int64_t row_stride,
+                                   const int32_t *lengths, const int32_t *row_starts,
+                                   const int32_t *offsets, int32_t k, int32_t *out)
+{
+    if (num_rows < 0 || width < 0 || row_stride < width || k < 1 || !offsets)
+        return OR_EINVAL;
+    int es = elem_size(dtype);
+    int32_t *raw = (int32_t *)malloc((size_t)k * sizeof(int32_t));
+    if (!raw)
+        return OR_ENOMEM;
+    for (int64_t r = 0; r < num_rows; ++r) {
+        int64_t rs = row_starts ? row_starts[r] : 0;
+        int64_t n = oracle_ragged_length(lengths[r], rs, width);
+        const char *row = (const char *)scores + (size_t)(r * row_stride + (n > 0 ? rs : 0)) * es;
+        int rc = oracle_select_row(row, dtype, n, k, raw, NULL);
+        if (rc != OR_OK) {
+            free(raw);
+            return rc;
+        }
+        for (int32_t s = 0; s < k; ++s) {
+            if (raw[s] < 0) {
+                out[r * k + s] = -1;
+                continue;
+            }
+            int64_t v = (int64_t)raw[s] + (int64_t)offsets[r];
+            if (v < INT32_MIN || v > INT32_MAX) {
+                free(raw);
+                return OR_ERANGE;
+            }
+            out[r * k + s] = (int32_t)v;
+        }
+    }
+    free(raw);
+    return OR_OK;
+}
+
+/* Page-table transform with page_size 1 over requests (SGLang TopK ops,
+ * fast_topk_transform_fused): row r belongs to request b with
+ * cu_seqlens_q[b] <= r < cu_seqlens_q[b + 1] (a row no request covers is
+ * empty), and each selected row-local index idx becomes page_table[b, idx]
+ * (-1 when idx >= pt_cols); -1 stays -1. */
+int oracle_seqs_page_table_transform(const void *scores, int dtype, int64_t num_rows,
+                                     int64_t width, int64_t row_stride,
+                                     const int32_t *lengths, const int32_t *row_starts,
+                                     const int32_t *page_table, int64_t pt_cols,
+                                     int64_t pt_row_stride, const int32_t *cu_seqlens_q,
+                                     int64_t num_reqs, int32_t k, int32_t *out)
+{
+    if (num_rows < 0 || width < 0 || row_stride < width || k < 1 || num_reqs < 0 ||
+        pt_cols < 0 || pt_row_stride < pt_cols || !cu_seqlens_q)
+        return OR_EINVAL;
+    int es = elem_size(dtype);
+    int32_t *raw = (int32_t *)malloc((size_t)k * sizeof(int32_t));
+    if (!raw)
+        return OR_ENOMEM;
+    for (int64_t r = 0; r < num_rows; ++r) {
+        int64_t b = -1;
+        for (int64_t q = 0; q < num_reqs; ++q)  /* plain linear search */
+            if (cu_seqlens_q[q] <= r && r < cu_seqlens_q[q + 1]) {
+                b = q;
+                break;
+            }
+        int64_t rs = row_starts ? row_starts[r] : 0;
+        int64_t n = b < 0 ? 0 : oracle_ragged_length(lengths[r], rs, width);
+        const char *row = (const char *)scores + (size_t)(r * row_stride + (n > 0 ? rs : 0)) * es;
+        int rc = oracle_select_row(row, dtype, n, k, raw, NULL);
+        if (rc != OR_OK) {
+            free(raw);
+            return rc;
+        }
+        for (int32_t s = 0; s < k; ++s) {
+            int32_t idx = raw[s];
+            out[r * k + s] = (idx < 0 || idx >= pt_cols) ? -1 : page_table[b * pt_row_stride + idx];
         }
     }
     free(raw);

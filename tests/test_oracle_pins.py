@@ -41,6 +41,12 @@ def _bind(lib):
     lib.oracle_page_table_transform.restype = ctypes.c_int
     lib.oracle_page_table_transform.argtypes = [
         vp, ctypes.c_int, i64, i64, i64, vp, vp, vp, i64, i64, vp, i32, i32, vp, vp]
+    lib.oracle_ragged_offset_transform.restype = ctypes.c_int
+    lib.oracle_ragged_offset_transform.argtypes = [
+        vp, ctypes.c_int, i64, i64, i64, vp, vp, vp, i32, vp]
+    lib.oracle_seqs_page_table_transform.restype = ctypes.c_int
+    lib.oracle_seqs_page_table_transform.argtypes = [
+        vp, ctypes.c_int, i64, i64, i64, vp, vp, vp, i64, i64, vp, i64, i32, vp]
     return lib
 
 
@@ -100,6 +106,33 @@ def golden_failures(lib):
             out.data_ptr(), raw.data_ptr())
         if rc != 0 or out.tolist() != case["out"] or raw.tolist() != case["out_raw"]:
             fails.append(f"page_table {case['name']}: rc={rc} {out.tolist()} {raw.tolist()}")
+    ep = _golden("epilogues.json")
+    for case in ep["ragged"]:
+        scores = torch.tensor([case["scores"]], dtype=torch.float32)
+        W = scores.shape[1]
+        lengths = torch.tensor([case["length"]], dtype=torch.int32)
+        rs = None if case["row_start"] is None else torch.tensor([case["row_start"]], dtype=torch.int32)
+        off = torch.tensor([case["offset"]], dtype=torch.int32)
+        k = case["k"]
+        out = torch.empty(k, dtype=torch.int32)
+        rc = lib.oracle_ragged_offset_transform(
+            scores.data_ptr(), 0, 1, W, W, lengths.data_ptr(),
+            rs.data_ptr() if rs is not None else None, off.data_ptr(), k, out.data_ptr())
+        if rc != 0 or out.tolist() != case["out"]:
+            fails.append(f"ragged {case['name']}: rc={rc} {out.tolist()}")
+    for case in ep["requests"]:
+        scores = torch.tensor(case["scores"], dtype=torch.float32)
+        R, W = scores.shape
+        lengths = torch.tensor(case["lengths"], dtype=torch.int32)
+        cu = torch.tensor(case["cu_seqlens_q"], dtype=torch.int32)
+        pt = torch.tensor(case["page_table"], dtype=torch.int32)
+        k = case["k"]
+        out = torch.empty(R, k, dtype=torch.int32)
+        rc = lib.oracle_seqs_page_table_transform(
+            scores.data_ptr(), 0, R, W, W, lengths.data_ptr(), None, pt.data_ptr(), pt.shape[1],
+            pt.shape[1], cu.data_ptr(), cu.numel() - 1, k, out.data_ptr())
+        if rc != 0 or out.tolist() != case["out"]:
+            fails.append(f"requests {case['name']}: rc={rc} {out.tolist()}")
     return fails
 
 
@@ -233,6 +266,11 @@ MUTANTS = [
     ("fp16 subnormal scale", "ldexp((double)fr, -24)", "ldexp((double)fr, -22)"),
     ("bf16 shift", "(uint32_t)h << 16", "(uint32_t)h << 15"),
     ("short rows not padded", "int64_t m = n < k ? n : k;", "int64_t m = k;"),
+    ("ragged offset subtracted", "int64_t v = (int64_t)raw[s] + (int64_t)offsets[r];",
+     "int64_t v = (int64_t)raw[s] - (int64_t)offsets[r];"),
+    ("request row dropped", "page_table[b * pt_row_stride + idx]", "page_table[idx]"),
+    ("request bounds off by one", "cu_seqlens_q[q] <= r && r < cu_seqlens_q[q + 1]",
+     "cu_seqlens_q[q] <= r && r <= cu_seqlens_q[q + 1]"),
 ]
 
 
@@ -256,3 +294,32 @@ def test_pins_catch_mutant(tmp_path, label, old, new):
         assert rc == 0, "the unmodified oracle must pass every pin in the child process"
     else:
         assert rc != 0, f"mutant '{label}' passed every pin"
+
+
+def test_epilogue_variants_brute_force(oracle_mod):
+    """The ragged-offset and request page-table epilogues against pure Python
+    (selection by sorted() on (-value, column), then the transform)."""
+    rnd = random.Random(11)
+    R, W, k = 9, 12, 5
+    vals = [[float(rnd.choice([-2, -1, 0, 1, 1, 2, 3, 5])) for _ in range(W)] for _ in range(R)]
+    scores = torch.tensor(vals, dtype=torch.float32)
+    lengths = [rnd.randint(0, W) for _ in range(R)]
+    starts = [rnd.randint(0, W - L) for L in lengths]
+    offsets = [rnd.randint(-50, 5000) for _ in range(R)]
+    cu = [0, 3, 3, 7]                       # rows 7, 8 belong to no request
+    pt = [[rnd.randint(0, 999) for _ in range(10)] for _ in range(3)]
+
+    def local_topk(r):
+        row = vals[r][starts[r]:starts[r] + lengths[r]]
+        return _brute(row, len(row), k)
+    out = oracle_mod.ragged_offset_transform(
+        scores, torch.tensor(lengths), torch.tensor(offsets), k, torch.tensor(starts))
+    for r in range(R):
+        assert out[r].tolist() == [i + offsets[r] if i >= 0 else -1 for i in local_topk(r)]
+    out2 = oracle_mod.seqs_page_table_transform(
+        scores, torch.tensor(lengths), torch.tensor(pt, dtype=torch.int32), torch.tensor(cu), k,
+        torch.tensor(starts))
+    for r in range(R):
+        b = next((q for q in range(len(cu) - 1) if cu[q] <= r < cu[q + 1]), None)
+        want = [-1] * k if b is None else [pt[b][i] if 0 <= i < 10 else -1 for i in local_topk(r)]
+        assert out2[r].tolist() == want
