@@ -143,6 +143,53 @@ int gbtopk_page_table_transform(const void *scores, int dtype, int64_t num_rows,
                                 size_t workspace_bytes, void *stream);
 
 /*
+ * gbtopk_ragged_transform — top-K fused with the ragged KV index offset.
+ *
+ * Defined by the SGLang TopK ops wiki, fast_topk_transform_ragged_fused
+ * ("top-k indices ... offset-adjusted for ragged KV layout", with
+ * topk_indices_offset of shape (B)): the selection is the one of
+ * gbtopk_page_table_transform's rows, and each selected row-local index idx
+ * is written as idx + topk_indices_offset[r] (modulo 2^32); -1 padding stays
+ * -1.
+ *
+ *  scores, lengths, row_starts, top_k, deterministic, workspace, stream:
+ *               as for gbtopk_page_table_transform (valid window
+ *               [row_start, row_start + length) clamped to the width).
+ *  topk_indices_offset  device int32 [num_rows].
+ *  out          device int32 [num_rows, top_k], 16-byte aligned.
+ */
+int gbtopk_ragged_transform(const void *scores, int dtype, int64_t num_rows, int64_t width,
+                            int64_t row_stride, const int32_t *lengths, const int32_t *row_starts,
+                            const int32_t *topk_indices_offset, int32_t top_k, int32_t *out,
+                            int deterministic, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * gbtopk_page_table_transform_cu_seqlens — top-K fused with a page_size-1
+ * page table indexed by request.
+ *
+ * Defined by the SGLang TopK ops wiki, fast_topk_transform_fused (page table
+ * with page_size 1 and cu_seqlens_q of shape (Batch + 1)): score row r
+ * belongs to request b with cu_seqlens_q[b] <= r < cu_seqlens_q[b + 1], and
+ * each selected row-local index idx is written as page_table[b, idx]; an idx
+ * at or beyond pt_cols gives -1, and a row that no request covers is empty
+ * (all -1).
+ *
+ *  scores, lengths, row_starts, top_k, deterministic, workspace, stream:
+ *               as for gbtopk_page_table_transform.
+ *  page_table   device int32 [num_reqs, pt_cols], inner stride 1, row stride
+ *               pt_row_stride entries.
+ *  cu_seqlens_q device int32 [num_reqs + 1], nondecreasing.
+ *  out          device int32 [num_rows, top_k], 16-byte aligned.
+ */
+int gbtopk_page_table_transform_cu_seqlens(const void *scores, int dtype, int64_t num_rows,
+                                           int64_t width, int64_t row_stride, const int32_t *lengths,
+                                           const int32_t *row_starts, const int32_t *page_table,
+                                           int64_t pt_cols, int64_t pt_row_stride,
+                                           const int32_t *cu_seqlens_q, int64_t num_reqs,
+                                           int32_t top_k, int32_t *out, int deterministic,
+                                           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * gbtopk_workspace_bytes — scratch needed by a call with this geometry.
  * A pure function of its arguments (capture-stable).  The workspace holds a
  * device status word plus, when rows are long enough to be split across

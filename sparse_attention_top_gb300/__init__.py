@@ -26,7 +26,8 @@ __all__ = [
     "top_k_varlen", "top_k_page_table_transform", "gbtopk_varlen",
     "gbtopk_page_table_transform", "gbtopk_workspace_bytes", "gbtopk_device_status",
     "gbtopk_plan_query", "gbtopk_status_str", "gbtopk_varlen_static_ws", "library_path",
-    "load_library",
+    "load_library", "top_k_ragged_transform", "top_k_page_table_transform_cu_seqlens",
+    "gbtopk_ragged_transform", "gbtopk_page_table_transform_cu_seqlens",
     "GbtopkError", "MAX_TOP_K",
 ]
 
@@ -81,6 +82,12 @@ def load_library():
         lib.gbtopk_varlen_static_ws.restype = c_int
         lib.gbtopk_varlen_static_ws.argtypes = [vp, c_int, i64, i64, i64, vp, i32, i32, i32, vp, vp,
                                                 vp, c_int, vp]
+        lib.gbtopk_ragged_transform.restype = c_int
+        lib.gbtopk_ragged_transform.argtypes = [vp, c_int, i64, i64, i64, vp, vp, vp, i32, vp,
+                                                c_int, vp, sz, vp]
+        lib.gbtopk_page_table_transform_cu_seqlens.restype = c_int
+        lib.gbtopk_page_table_transform_cu_seqlens.argtypes = [
+            vp, c_int, i64, i64, i64, vp, vp, vp, i64, i64, vp, i64, i32, vp, c_int, vp, sz, vp]
         lib.gbtopk_status_str.restype = ctypes.c_char_p
         lib.gbtopk_status_str.argtypes = [c_int]
         _lib = lib
@@ -170,6 +177,38 @@ def gbtopk_page_table_transform(scores: torch.Tensor, lengths: torch.Tensor,
         _ptr(scores), _DTYPES[scores.dtype], R, W, stride, _ptr(lengths), _ptr(row_starts),
         _ptr(page_table), P, pstride, _ptr(page_table_row_starts), page_size, top_k, _ptr(out),
         _ptr(out_raw), 1 if deterministic else 0, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), s))
+
+
+def gbtopk_ragged_transform(scores: torch.Tensor, lengths: torch.Tensor,
+                            row_starts: Optional[torch.Tensor], topk_indices_offset: torch.Tensor,
+                            top_k: int, out: torch.Tensor, deterministic: bool,
+                            workspace: torch.Tensor, stream=None) -> int:
+    """Direct call of the C entry point on tensors."""
+    R, W = scores.shape
+    stride = scores.stride(0) if R > 1 else W
+    s = _stream_handle(scores.device) if stream is None else stream
+    return _check(load_library().gbtopk_ragged_transform(
+        _ptr(scores), _DTYPES[scores.dtype], R, W, stride, _ptr(lengths), _ptr(row_starts),
+        _ptr(topk_indices_offset), top_k, _ptr(out), 1 if deterministic else 0, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), s))
+
+
+def gbtopk_page_table_transform_cu_seqlens(scores: torch.Tensor, lengths: torch.Tensor,
+                                           row_starts: Optional[torch.Tensor],
+                                           page_table: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                                           top_k: int, out: torch.Tensor, deterministic: bool,
+                                           workspace: torch.Tensor, stream=None) -> int:
+    """Direct call of the C entry point on tensors."""
+    R, W = scores.shape
+    stride = scores.stride(0) if R > 1 else W
+    P = page_table.shape[1]
+    pstride = page_table.stride(0) if page_table.shape[0] > 1 else P
+    s = _stream_handle(scores.device) if stream is None else stream
+    return _check(load_library().gbtopk_page_table_transform_cu_seqlens(
+        _ptr(scores), _DTYPES[scores.dtype], R, W, stride, _ptr(lengths), _ptr(row_starts),
+        _ptr(page_table), P, pstride, _ptr(cu_seqlens_q), cu_seqlens_q.numel() - 1, top_k,
+        _ptr(out), 1 if deterministic else 0, _ptr(workspace),
         workspace.numel() * workspace.element_size(), s))
 
 
@@ -294,3 +333,62 @@ def top_k_page_table_transform(scores: torch.Tensor, lengths: torch.Tensor,
     gbtopk_page_table_transform(scores, lengths, row_starts, page_table, page_table_row_starts,
                                 page_size, top_k, o, raw, deterministic, ws)
     return (o, raw) if raw is not None else o
+
+
+def _ragged_inputs(scores, lengths, row_starts, name_tensors):
+    for t, name in name_tensors:
+        _require_cuda(t, name)
+    if scores.dim() != 2 or scores.stride(1) != 1 or scores.dtype not in _DTYPES:
+        raise ValueError("scores must be a 2-D fp32/bf16/fp16 tensor with inner stride 1")
+    R = scores.shape[0]
+    for t, name in ((lengths, "lengths"), (row_starts, "row_starts")):
+        if t is not None and (t.dtype != torch.int32 or t.numel() != R or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous int32 tensor of num_rows")
+
+
+def top_k_ragged_transform(scores: torch.Tensor, lengths: torch.Tensor,
+                           topk_indices_offset: torch.Tensor, top_k: int,
+                           row_starts: Optional[torch.Tensor] = None,
+                           out: Optional[torch.Tensor] = None, deterministic: bool = False,
+                           workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Top-k fused with the ragged KV index offset (SGLang
+    fast_topk_transform_ragged_fused): out = idx + topk_indices_offset[row]."""
+    _ragged_inputs(scores, lengths, row_starts,
+                   ((scores, "scores"), (lengths, "lengths"),
+                    (topk_indices_offset, "topk_indices_offset")))
+    R, W = scores.shape
+    if (topk_indices_offset.dtype != torch.int32 or topk_indices_offset.numel() != R
+            or not topk_indices_offset.is_contiguous()):
+        raise ValueError("topk_indices_offset must be a contiguous int32 tensor of num_rows")
+    o = _out_view(out, R, top_k, torch.int32, scores.device, "out")
+    ws = workspace if workspace is not None else _workspace(
+        scores.device, gbtopk_workspace_bytes(R, W, top_k, scores.dtype))
+    gbtopk_ragged_transform(scores, lengths, row_starts, topk_indices_offset, top_k, o,
+                            deterministic, ws)
+    return o
+
+
+def top_k_page_table_transform_cu_seqlens(scores: torch.Tensor, lengths: torch.Tensor,
+                                          page_table: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                                          top_k: int, row_starts: Optional[torch.Tensor] = None,
+                                          out: Optional[torch.Tensor] = None,
+                                          deterministic: bool = False,
+                                          workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Top-k fused with a page_size-1 page table indexed by request (SGLang
+    fast_topk_transform_fused): row r of request b (cu_seqlens_q[b] <= r <
+    cu_seqlens_q[b + 1]) gets page_table[b, idx]."""
+    _ragged_inputs(scores, lengths, row_starts,
+                   ((scores, "scores"), (lengths, "lengths"), (page_table, "page_table"),
+                    (cu_seqlens_q, "cu_seqlens_q")))
+    R, W = scores.shape
+    if page_table.dim() != 2 or page_table.stride(1) != 1 or page_table.dtype != torch.int32:
+        raise ValueError("page_table must be an int32 [num_reqs, pt_cols] tensor, inner stride 1")
+    if (cu_seqlens_q.dtype != torch.int32 or cu_seqlens_q.dim() != 1
+            or cu_seqlens_q.numel() != page_table.shape[0] + 1 or not cu_seqlens_q.is_contiguous()):
+        raise ValueError("cu_seqlens_q must be a contiguous int32 tensor of num_reqs + 1")
+    o = _out_view(out, R, top_k, torch.int32, scores.device, "out")
+    ws = workspace if workspace is not None else _workspace(
+        scores.device, gbtopk_workspace_bytes(R, W, top_k, scores.dtype))
+    gbtopk_page_table_transform_cu_seqlens(scores, lengths, row_starts, page_table, cu_seqlens_q,
+                                           top_k, o, deterministic, ws)
+    return o

@@ -169,6 +169,72 @@ int gbtopk_varlen(const void *logits, int dtype, int64_t num_rows, int64_t width
     return rc != GBTOPK_OK ? rc : status;
 }
 
+int gbtopk_ragged_transform(const void *scores, int dtype, int64_t num_rows, int64_t width,
+                            int64_t row_stride, const int32_t *lengths, const int32_t *row_starts,
+                            const int32_t *topk_indices_offset, int32_t top_k, int32_t *out,
+                            int deterministic, void *workspace, size_t workspace_bytes, void *stream) {
+    if (num_rows < 0) return GBTOPK_EINVAL;
+    Plan plan;
+    int rc = check_common(scores, dtype, num_rows, width, row_stride, top_k, out, workspace,
+                          workspace_bytes, &plan);
+    if (rc != GBTOPK_OK || num_rows == 0) return rc;
+    if (!lengths || !topk_indices_offset) return GBTOPK_EINVAL;
+    Params p{};
+    p.x = scores;
+    p.num_rows = num_rows;
+    p.width = width;
+    p.row_stride = num_rows > 1 ? row_stride : (row_stride > width ? row_stride : width);
+    p.next_n = 1;
+    p.compress_ratio = 1;
+    p.lengths = lengths;
+    p.row_starts = row_starts;
+    p.k = top_k;
+    p.deterministic = deterministic ? 1 : 0;
+    p.out_idx = out;
+    p.idx_offset = topk_indices_offset;
+    p.page_size = 1;
+    p.ws = static_cast<uint8_t *>(workspace);
+    p.plan = plan;
+    return launch(dtype, p, stream);
+}
+
+int gbtopk_page_table_transform_cu_seqlens(const void *scores, int dtype, int64_t num_rows,
+                                           int64_t width, int64_t row_stride, const int32_t *lengths,
+                                           const int32_t *row_starts, const int32_t *page_table,
+                                           int64_t pt_cols, int64_t pt_row_stride,
+                                           const int32_t *cu_seqlens_q, int64_t num_reqs,
+                                           int32_t top_k, int32_t *out, int deterministic,
+                                           void *workspace, size_t workspace_bytes, void *stream) {
+    if (num_rows < 0 || num_reqs < 0 || pt_cols < 0) return GBTOPK_EINVAL;
+    if (num_reqs > 1 && pt_row_stride < pt_cols) return GBTOPK_EINVAL;
+    Plan plan;
+    int rc = check_common(scores, dtype, num_rows, width, row_stride, top_k, out, workspace,
+                          workspace_bytes, &plan);
+    if (rc != GBTOPK_OK || num_rows == 0) return rc;
+    if (!lengths || !page_table || !cu_seqlens_q) return GBTOPK_EINVAL;
+    Params p{};
+    p.x = scores;
+    p.num_rows = num_rows;
+    p.width = width;
+    p.row_stride = num_rows > 1 ? row_stride : (row_stride > width ? row_stride : width);
+    p.next_n = 1;
+    p.compress_ratio = 1;
+    p.lengths = lengths;
+    p.row_starts = row_starts;
+    p.k = top_k;
+    p.deterministic = deterministic ? 1 : 0;
+    p.out_idx = out;
+    p.page_table = page_table;
+    p.pt_cols = pt_cols;
+    p.pt_row_stride = num_reqs > 1 ? pt_row_stride : (pt_row_stride > pt_cols ? pt_row_stride : pt_cols);
+    p.page_size = 1;
+    p.cu_seqlens_q = cu_seqlens_q;
+    p.num_reqs = num_reqs;
+    p.ws = static_cast<uint8_t *>(workspace);
+    p.plan = plan;
+    return launch(dtype, p, stream);
+}
+
 int gbtopk_page_table_transform(const void *scores, int dtype, int64_t num_rows, int64_t width,
                                 int64_t row_stride, const int32_t *lengths,
                                 const int32_t *row_starts, const int32_t *page_table,

@@ -70,6 +70,9 @@ struct Params {
     const int32_t *pt_row_starts;
     int32_t page_size;
     int32_t pt_start_is_row_start;
+    const int32_t *idx_offset;    // ragged KV: out = idx + idx_offset[row] (null: none)
+    const int32_t *cu_seqlens_q;  // page-table row = request of the score row (null: the row itself)
+    int64_t num_reqs;
     uint8_t *ws;   // status word at ws[0]; per-row blocks from kWsHeaderBytes
     int64_t row0;  // first row of this launch (the split pipeline runs in row blocks)
     int64_t rows;  // rows of this launch

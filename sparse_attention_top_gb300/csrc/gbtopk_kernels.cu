@@ -457,7 +457,26 @@ __device__ void exact_select(const S &s, int64_t n, int k, bool det, uint2 *sel,
 
 // ---------------------------------------------------------------- row geometry and output
 
+// Request b of a score row when rows are grouped by cu_seqlens_q
+// (cu_seqlens_q[b] <= row < cu_seqlens_q[b + 1]), or -1 when none covers it.
+__device__ __forceinline__ int64_t request_of(const Params &p, int64_t row) {
+    int64_t lo = 0, hi = p.num_reqs;  // first b in [0, num_reqs] with cu[b] > row
+    while (lo < hi) {
+        const int64_t mid = (lo + hi) >> 1;
+        if (static_cast<int64_t>(__ldg(p.cu_seqlens_q + mid)) <= row) lo = mid + 1;
+        else hi = mid;
+    }
+    const int64_t b = lo - 1;
+    if (b < 0 || b >= p.num_reqs || row >= static_cast<int64_t>(__ldg(p.cu_seqlens_q + b + 1))) return -1;
+    return b;
+}
+
 __device__ __forceinline__ void row_window(const Params &p, int64_t row, int64_t &n, int64_t &col0) {
+    if (p.cu_seqlens_q && request_of(p, row) < 0) {  // no request: an empty row
+        n = 0;
+        col0 = 0;
+        return;
+    }
     if (p.seq_lens) {
         const int64_t i = row / p.next_n, t = row % p.next_n;
         const int64_t num = static_cast<int64_t>(__ldg(p.seq_lens + i)) - p.next_n + t + 1;
@@ -477,47 +496,63 @@ __device__ __forceinline__ void row_window(const Params &p, int64_t row, int64_t
     }
 }
 
-// One output slot j of `row`: the index (page-table transformed when a
-// table is given, the raw index then going to out_raw) and the value
-// (bit copy, or the dtype's lowest finite value for a -1 slot).
+// Per-row context of the index epilogue: the page-table row and first
+// entry (compact page table: the score row and its start; request page
+// table: the request, start 0), or the ragged KV offset.
+struct RowEpi {
+    int64_t pt_row, pt_start;
+    int32_t offset;
+};
+
+__device__ __forceinline__ RowEpi row_epilogue(const Params &p, int64_t row) {
+    RowEpi e{row, 0, 0};
+    if (p.idx_offset) e.offset = __ldg(p.idx_offset + row);
+    if (p.page_table) {
+        if (p.cu_seqlens_q) {
+            e.pt_row = request_of(p, row);  // rows no request covers are empty
+        } else if (p.pt_row_starts) {
+            e.pt_start = __ldg(p.pt_row_starts + row);
+        } else if (p.pt_start_is_row_start) {
+            e.pt_start = __ldg(p.row_starts + row);
+        }
+    }
+    return e;
+}
+
+// The output index of a selected row-local index idx (-1 stays -1): idx
+// itself, idx + the ragged offset, or its page-table translation
+// page_table[pt_row, pt_start + idx / page_size] * page_size + idx % page_size
+// (-1 for a column outside the table; modulo 2^32).
+__device__ __forceinline__ int32_t out_index(const Params &p, const RowEpi &e, int32_t idx) {
+    if (idx < 0) return -1;
+    if (p.idx_offset) return static_cast<int32_t>(static_cast<uint32_t>(idx) + static_cast<uint32_t>(e.offset));
+    if (!p.page_table) return idx;
+    const int64_t col = e.pt_start + idx / p.page_size;
+    if (col < 0 || col >= p.pt_cols) return -1;
+    const int64_t page = __ldg(p.page_table + e.pt_row * p.pt_row_stride + col);
+    return static_cast<int32_t>(static_cast<uint32_t>(static_cast<uint64_t>(page * p.page_size + idx % p.page_size)));
+}
+
+// One output slot j of `row`: the output index, the raw index in out_raw
+// (when given), and the value (bit copy, or the dtype's lowest finite value
+// for a -1 slot).
 template <int DT>
-__device__ __forceinline__ void put_slot(const Params &p, int64_t row, int64_t pt_start, int j, int32_t idx,
+__device__ __forceinline__ void put_slot(const Params &p, int64_t row, const RowEpi &e, int j, int32_t idx,
                                          uint32_t raw) {
     using raw_t = typename Elem<DT>::raw_t;
     const int k = p.k;
-    int32_t *out = p.out_idx + row * k;
-    if (p.page_table) {
-        int32_t v = -1;
-        if (idx >= 0) {
-            const int64_t col = pt_start + idx / p.page_size;
-            if (col >= 0 && col < p.pt_cols) {
-                const int64_t page = __ldg(p.page_table + row * p.pt_row_stride + col);
-                v = static_cast<int32_t>(static_cast<uint32_t>(
-                    static_cast<uint64_t>(page * p.page_size + idx % p.page_size)));
-            }
-        }
-        out[j] = v;
-        if (p.out_raw) p.out_raw[row * k + j] = idx;
-    } else {
-        out[j] = idx;
-    }
+    p.out_idx[row * k + j] = out_index(p, e, idx);
+    if (p.out_raw) p.out_raw[row * k + j] = idx;
     if (p.out_val)
         static_cast<raw_t *>(p.out_val)[row * k + j] = static_cast<raw_t>(idx >= 0 ? raw : Elem<DT>::kLowest);
 }
 
-__device__ __forceinline__ int64_t page_table_start(const Params &p, int64_t row) {
-    if (!p.page_table) return 0;
-    if (p.pt_row_starts) return __ldg(p.pt_row_starts + row);
-    if (p.pt_start_is_row_start) return __ldg(p.row_starts + row);
-    return 0;
-}
-
 template <int DT>
 __device__ void emit(const Params &p, int64_t row, const uint2 *sel, int m) {
-    const int64_t pt_start = page_table_start(p, row);
+    const RowEpi ep = row_epilogue(p, row);
     for (int j = threadIdx.x; j < p.k; j += blockDim.x) {
         const bool live = j < m;
-        put_slot<DT>(p, row, pt_start, j, live ? static_cast<int32_t>(sel[j].y) : -1, live ? sel[j].x : 0u);
+        put_slot<DT>(p, row, ep, j, live ? static_cast<int32_t>(sel[j].y) : -1, live ? sel[j].x : 0u);
     }
 }
 
@@ -534,7 +569,7 @@ __device__ void emit_sorted(const Params &p, int64_t row, const uint2 *sel, int 
     uint2 *seg = reinterpret_cast<uint2 *>(scratch + kBins * 4);
     const int nt = blockDim.x;
     const int tid = threadIdx.x;
-    const int64_t pt_start = page_table_start(p, row);
+    const RowEpi ep = row_epilogue(p, row);
     if (tid == 0) {
         c.key_min = 0xFFFFFFFFu;
         c.key_max = 0;
@@ -588,9 +623,9 @@ __device__ void emit_sorted(const Params &p, int64_t row, const uint2 *sel, int 
                                           static_cast<unsigned long long>(0xFFFFFFFFu - o.y);
             before += oc > mine ? 1u : 0u;
         }
-        put_slot<DT>(p, row, pt_start, static_cast<int>(lo + before), static_cast<int32_t>(v.y), v.x);
+        put_slot<DT>(p, row, ep, static_cast<int>(lo + before), static_cast<int32_t>(v.y), v.x);
     }
-    for (int j = m + tid; j < p.k; j += nt) put_slot<DT>(p, row, pt_start, j, -1, 0u);
+    for (int j = m + tid; j < p.k; j += nt) put_slot<DT>(p, row, ep, j, -1, 0u);
     __syncthreads();
 }
 
@@ -1757,31 +1792,18 @@ __global__ void __launch_bounds__(128) small_kernel(const __grid_constant__ Para
             tie_base += __popc(bt);
         }
     }
-    if (!p.page_table && !p.out_val) return;
+    if (!p.page_table && !p.idx_offset && !p.out_val) return;
     __syncwarp();  // the warp's index stores are visible to its lanes
-    int64_t pt_start = 0;
-    if (p.page_table) {
-        if (p.pt_row_starts) pt_start = __ldg(p.pt_row_starts + row);
-        else if (p.pt_start_is_row_start) pt_start = __ldg(p.row_starts + row);
-    }
+    const RowEpi ep = row_epilogue(p, row);
 #pragma unroll 1
     for (int64_t j = lane; j < k; j += 32) {
         const int32_t idx = out[j];
         if (p.out_val)
             static_cast<raw_t *>(p.out_val)[row * k + j] =
                 static_cast<raw_t>(idx >= 0 ? ldg_raw(xrow + idx) : Elem<DT>::kLowest);
-        if (p.page_table) {
-            int32_t v = -1;
-            if (idx >= 0) {
-                const int64_t col = pt_start + idx / p.page_size;
-                if (col >= 0 && col < p.pt_cols) {
-                    const int64_t page = __ldg(p.page_table + row * p.pt_row_stride + col);
-                    v = static_cast<int32_t>(static_cast<uint32_t>(
-                        static_cast<uint64_t>(page * p.page_size + idx % p.page_size)));
-                }
-            }
+        if (p.page_table || p.idx_offset) {
             if (p.out_raw) p.out_raw[row * k + j] = idx;
-            out[j] = v;
+            out[j] = out_index(p, ep, idx);
         }
     }
 }

@@ -150,3 +150,51 @@ def test_no_cpu_path():
     x = torch.randn(2, 64)
     with pytest.raises(ValueError):
         gb.top_k_varlen(x, torch.tensor([64, 64], dtype=torch.int32), 8)
+
+
+def _ragged(**kw):
+    lib = gb.load_library()
+    a = dict(scores=A, dtype=0, num_rows=2, width=64, row_stride=64, lengths=A + 4096,
+             row_starts=None, offsets=A + 8192, top_k=8, out=A + 16384, det=0, ws=WS,
+             ws_bytes=1 << 20, stream=None)
+    a.update(kw)
+    return lib.gbtopk_ragged_transform(
+        a["scores"], a["dtype"], a["num_rows"], a["width"], a["row_stride"], a["lengths"],
+        a["row_starts"], a["offsets"], a["top_k"], a["out"], a["det"], a["ws"], a["ws_bytes"],
+        a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(offsets=None), gb.EINVAL),
+    (dict(lengths=None), gb.EINVAL),
+    (dict(out=A + 16388), gb.EALIGN),
+    (dict(top_k=4096), gb.EUNSUPPORTED),
+    (dict(ws_bytes=0), gb.EWORKSPACE),
+])
+def test_ragged_argument_checks(kw, status):
+    assert _ragged(**kw) == status
+
+
+def _cu(**kw):
+    lib = gb.load_library()
+    a = dict(scores=A, dtype=0, num_rows=3, width=64, row_stride=64, lengths=A + 4096,
+             row_starts=None, page_table=A + 8192, pt_cols=16, pt_row_stride=16,
+             cu=A + 12288, num_reqs=2, top_k=8, out=A + 16384, det=0, ws=WS, ws_bytes=1 << 20,
+             stream=None)
+    a.update(kw)
+    return lib.gbtopk_page_table_transform_cu_seqlens(
+        a["scores"], a["dtype"], a["num_rows"], a["width"], a["row_stride"], a["lengths"],
+        a["row_starts"], a["page_table"], a["pt_cols"], a["pt_row_stride"], a["cu"],
+        a["num_reqs"], a["top_k"], a["out"], a["det"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(cu=None), gb.EINVAL),
+    (dict(page_table=None), gb.EINVAL),
+    (dict(num_reqs=-1), gb.EINVAL),
+    (dict(pt_row_stride=8), gb.EINVAL),
+    (dict(out=A + 16388), gb.EALIGN),
+    (dict(ws=None), gb.EWORKSPACE),
+])
+def test_cu_seqlens_argument_checks(kw, status):
+    assert _cu(**kw) == status

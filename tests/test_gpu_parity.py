@@ -388,3 +388,84 @@ def test_page_table_noncontiguous_table_and_no_raw(dev):
         return big[:, :P]
     _run_page_table(dev, c, pt_view=wide)
     _run_page_table(dev, c, pt_view=wide, with_raw=False)
+
+
+# ------------------------------------------------------------------ other epilogues (SGLang ops)
+
+def _ragged_case(R, W, seed, dtype=torch.float32, stride=None):
+    g = torch.Generator().manual_seed(seed)
+    S = stride or W
+    storage = torch.full((R, S), 3.0e38)
+    storage[:, :W] = torch.randn(R, W, generator=g)
+    scores = storage[:, :W].to(dtype) if dtype != torch.float32 else storage[:, :W]
+    lengths = torch.randint(0, W + 1, (R,), generator=g, dtype=torch.int32)
+    lengths[0] = 0
+    starts = torch.stack([torch.randint(0, W - int(L) + 1, (1,), generator=g)[0] for L in lengths])
+    return scores, lengths, starts.to(torch.int32)
+
+
+def _to_dev_strided(x, dev):
+    R, W = x.shape
+    S = x.stride(0)
+    base = torch.empty(R, S, dtype=x.dtype, device=dev)
+    base.copy_(torch.as_strided(x, (R, S), (S, 1)))
+    return base[:, :W]
+
+
+@pytest.mark.parametrize("R,W,k,det", [(64, 1500, 256, False), (48, 40000, 2048, False),
+                                       (48, 40000, 2048, True), (3, 300000, 512, False)])
+def test_ragged_offset_transform(dev, R, W, k, det):
+    scores, lengths, starts = _ragged_case(R, W, 6000 + W, stride=W + 13)
+    g = torch.Generator().manual_seed(7)
+    offsets = torch.randint(-1000, 10_000_000, (R,), generator=g, dtype=torch.int32)
+    out = gb.top_k_ragged_transform(_to_dev_strided(scores, dev), lengths.to(dev),
+                                    offsets.to(dev), k, row_starts=starts.to(dev),
+                                    deterministic=det)
+    torch.cuda.synchronize(dev)
+    ref = oracle.ragged_offset_transform(scores, lengths, offsets, k, starts)
+    if det:
+        assert torch.equal(out.cpu(), ref)
+    else:   # tie-aware: back to row-local indices, then the usual checks
+        raw = out.cpu().clone()
+        live = raw >= 0
+        raw[live] -= offsets.view(-1, 1).expand_as(raw)[live]
+        refraw = ref.clone()
+        refraw[ref >= 0] -= offsets.view(-1, 1).expand_as(ref)[ref >= 0]
+        n = [oracle.ragged_length(int(lengths[r]), int(starts[r]), W) for r in range(R)]
+        check_rows(scores, n, k, raw, refraw, None, col0=starts.tolist())
+
+
+@pytest.mark.parametrize("R,W,k,det", [(40, 1800, 512, False), (40, 50000, 2048, False),
+                                       (40, 50000, 2048, True)])
+def test_page_table_cu_seqlens(dev, R, W, k, det):
+    scores, lengths, starts = _ragged_case(R, W, 7000 + W)
+    g = torch.Generator().manual_seed(9)
+    cu = torch.tensor([0, 5, 5, 17, 30, 36], dtype=torch.int32)   # rows 36.. belong to none
+    B = cu.numel() - 1
+    P = W - 100                                                   # some indices fall past the table
+    # distinct entries, so an output identifies its column
+    full = torch.stack([torch.randperm(P + 24, generator=g) + b * 10_000_000 for b in range(B)])
+    pt = full.to(torch.int32)[:, :P]
+    out = gb.top_k_page_table_transform_cu_seqlens(
+        scores.to(dev), lengths.to(dev), _to_dev_strided(pt, dev), cu.to(dev), k,
+        row_starts=starts.to(dev), deterministic=det)
+    torch.cuda.synchronize(dev)
+    ref = oracle.seqs_page_table_transform(scores, lengths, pt.contiguous(), cu, k, starts)
+    if det:
+        assert torch.equal(out.cpu(), ref)
+        return
+    o = out.cpu()
+    for r in range(R):   # tie-aware: decode entries back to columns, compare value multisets
+        b = next((q for q in range(B) if int(cu[q]) <= r < int(cu[q + 1])), None)
+        if b is None:
+            assert bool((o[r] == -1).all())
+            continue
+        inv = {int(v): j for j, v in enumerate(pt[b].tolist())}
+        rs = int(starts[r])
+
+        def vals(row_out):
+            got = [inv[int(v)] for v in row_out.tolist() if v != -1]
+            assert len(set(got)) == len(got), f"row {r}: duplicate columns"
+            return sorted(float(scores[r, rs + j]) for j in got)
+        assert int((o[r] == -1).sum()) == int((ref[r] == -1).sum()), f"row {r}: -1 count"
+        assert vals(o[r]) == vals(ref[r]), f"row {r}: selected values differ"
