@@ -994,6 +994,9 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
     (void)kTraceBase;
 
     GBTOPK_TRACE_POINT(0, 0);
+    // launched as a programmatic dependent of whatever ran before on the
+    // stream: no input is read before that kernel has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     int64_t n, col0;
     row_window(p, row, n, col0);
     const raw_t *xrow = static_cast<const raw_t *>(p.x) + row * p.row_stride + col0;
@@ -1685,6 +1688,9 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
     }
     if (fallback) exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, det, sel, c.rhist, c);
     GBTOPK_TRACE_POINT(2, 0);
+    // the next call's first kernel may launch now (it waits for this grid
+    // to complete before reading anything)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (!copy_ok && tid == 0) mbar_wait(&c.bar, 0);  // let the copies land (before reusing cand)
     if (det) {
         __syncthreads();
@@ -1713,6 +1719,9 @@ __global__ void __launch_bounds__(128) small_kernel(const __grid_constant__ Para
     constexpr int KB = Elem<DT>::kKeyBits;
     const uint32_t lane = lane_id();
     __shared__ uint32_t small_hist[4 * 256];  // one digit histogram per warp
+    // a programmatic dependent of the stream's preceding kernel (see the
+    // row kernel); the next call may launch once every row is selected
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
     if (row >= p.num_rows) return;  // whole warps
     const int k = p.k;
@@ -1792,6 +1801,7 @@ __global__ void __launch_bounds__(128) small_kernel(const __grid_constant__ Para
             tie_base += __popc(bt);
         }
     }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (!p.page_table && !p.idx_offset && !p.out_val) return;
     __syncwarp();  // the warp's index stores are visible to its lanes
     const RowEpi ep = row_epilogue(p, row);
@@ -1811,8 +1821,16 @@ __global__ void __launch_bounds__(128) small_kernel(const __grid_constant__ Para
 template <int DT, int NE>
 cudaError_t launch_small(const Params &p, cudaStream_t stream) {
     const unsigned grid = static_cast<unsigned>((p.num_rows + 3) / 4);
-    small_kernel<DT, NE><<<grid, 128, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(128);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, small_kernel<DT, NE>, p);
 }
 
 template <class K>
@@ -1832,8 +1850,17 @@ cudaError_t launch_row(const Params &p, cudaStream_t stream) {
     const size_t bytes = p.plan.row_smem + (p.deterministic ? kDetScratchBytes : 0);
     const cudaError_t e = set_smem(row_kernel<DT, VPT>, bytes, configured);
     if (e != cudaSuccess) return e;
-    row_kernel<DT, VPT><<<static_cast<unsigned>(p.rows), kThreads, bytes, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.rows));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, row_kernel<DT, VPT>, p);
 }
 
 // Row-kernel variant by the vectors each thread holds for a direct row.
