@@ -469,3 +469,37 @@ def test_page_table_cu_seqlens(dev, R, W, k, det):
             return sorted(float(scores[r, rs + j]) for j in got)
         assert int((o[r] == -1).sum()) == int((ref[r] == -1).sum()), f"row {r}: -1 count"
         assert vals(o[r]) == vals(ref[r]), f"row {r}: selected values differ"
+
+
+# ------------------------------------------------------------------ size limits
+
+def test_more_rows_than_one_launch(dev):
+    """More split rows than one stream launch takes (2048): the call runs the
+    row / stream / finalize chain per block of rows; sampled rows from both
+    blocks and the block edges are checked."""
+    g = torch.Generator().manual_seed(8100)
+    R, W, k = 2100, 20000, 256
+    x = torch.randn(R, W, generator=g)
+    lens = torch.randint(k - 10, W + 1, (R,), generator=g, dtype=torch.int32)
+    c = workloads.VarlenCase("many_rows", x, lens, k)
+    run_case(dev, c, rows=[0, 1, 1000, 2046, 2047, 2048, 2049, 2099], poison=False, values=False)
+
+
+@pytest.mark.parametrize("k", [1, 2048])
+def test_widest_rows(dev, k):
+    """Rows of 4 M fp32 columns (512 chunks, the plan's limit): most of a row's
+    candidates overflow the shared gather buffer, so the finalize takes the
+    two-pass path over the segments in L2."""
+    g = torch.Generator().manual_seed(8200 + k)
+    W = 512 * 8192
+    x = torch.randn(2, W, generator=g)
+    x[1, ::1000] += 5.0                                  # a heavy tail in row 1
+    c = workloads.VarlenCase("widest", x, torch.tensor([W, W - 12345], dtype=torch.int32), k)
+    run_case(dev, c, poison=False)
+    assert gb.gbtopk_plan_query(2, W, k, torch.float32)["chunks_per_row"] == 512
+
+
+def test_wider_than_the_plan_is_refused(dev):
+    W = 512 * 8192 + 1
+    with pytest.raises(gb.GbtopkError):
+        gb.gbtopk_plan_query(1, W, 64, torch.float32)
