@@ -58,6 +58,11 @@ def _load():
             lib.oracle_page_table_transform.argtypes = [
                 vp, ctypes.c_int, i64, i64, i64, vp, vp, vp, i64, i64, vp, i32, i32,
                 vp, vp]
+            lib.oracle_topk_varlen_ties.restype = ctypes.c_int
+            lib.oracle_topk_varlen_ties.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp,
+                                                    i32, i32, i32, ctypes.c_int, vp, vp]
+            lib.oracle_select_row_large_ties.restype = ctypes.c_int
+            lib.oracle_select_row_large_ties.argtypes = [vp, ctypes.c_int, i64, i32, vp, vp]
             lib.oracle_ragged_offset_transform.restype = ctypes.c_int
             lib.oracle_ragged_offset_transform.argtypes = [
                 vp, ctypes.c_int, i64, i64, i64, vp, vp, vp, i32, vp]
@@ -129,6 +134,25 @@ def topk_varlen(logits, seq_lens, top_k: int, next_n: int = 1, compress_ratio: i
                                     _ptr(val))
     if rc != 0:
         raise ValueError(f"oracle_topk_varlen failed: {rc}")
+    return idx, val
+
+
+def topk_varlen_ties(logits, seq_lens, top_k: int, tie_large: bool, next_n: int = 1,
+                     compress_ratio: int = 1, return_values: bool = True):
+    """Oracle of `top_k_varlen` with a tie mode (SMALL: smallest columns among
+    the values equal to the k-th; LARGE: largest), canonical output order."""
+    import torch
+    assert logits.dim() == 2 and logits.stride(1) == 1 and logits.device.type == "cpu"
+    R, W = logits.shape
+    S = logits.stride(0) if R > 1 else W
+    sl = seq_lens.to(torch.int32).contiguous()
+    idx = torch.empty((R, top_k), dtype=torch.int32)
+    val = torch.empty((R, top_k), dtype=logits.dtype) if return_values else None
+    rc = _load().oracle_topk_varlen_ties(_ptr(logits), DTYPE_CODES[_dtype_name(logits)], R, W, S,
+                                         _ptr(sl), next_n, compress_ratio, top_k,
+                                         1 if tie_large else 0, _ptr(idx), _ptr(val))
+    if rc != 0:
+        raise ValueError(f"oracle_topk_varlen_ties failed: {rc}")
     return idx, val
 
 

@@ -51,6 +51,12 @@
  * Readings: idx is the row-local index in both (relative to row_start); a
  * row no request covers is empty (all -1); an idx at or beyond pt_cols
  * yields -1; idx + offset must fit in int32 (error otherwise).
+ *
+ * Tie selection (FlashInfer compact page-table PR body: "SMALL/LARGE tie
+ * selection", independent of the canonical output-order sort): SMALL keeps,
+ * among values equal to the k-th, the smallest columns (the selection
+ * above); LARGE keeps the largest.  The kept set is reported in the
+ * canonical (value desc, index asc) order in both modes.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -179,6 +185,79 @@ int oracle_select_row(const void *row, int dtype, int64_t n, int32_t k,
 
 /* The whole batch of FlashInfer `top_k_varlen`: logits [num_rows, width]
  * with row stride `row_stride` elements; seq_lens [num_rows / next_n]. */
+static int by_value_desc_index_desc(const void *a, const void *b)
+{
+    const item_t *x = (const item_t *)a;
+    const item_t *y = (const item_t *)b;
+    if (x->v > y->v)
+        return -1;
+    if (x->v < y->v)
+        return 1;
+    return (x->j > y->j) ? -1 : (x->j < y->j ? 1 : 0);
+}
+
+/* Top-k of one row with LARGE ties: the first min(k, n) columns in
+ * (value desc, index desc) order are kept, then reported in the canonical
+ * (value desc, index asc) order; padding as for oracle_select_row. */
+int oracle_select_row_large_ties(const void *row, int dtype, int64_t n, int32_t k,
+                                 int32_t *out_idx, void *out_val)
+{
+    if (k < 1 || n < 0 || (dtype != OR_F32 && dtype != OR_BF16 && dtype != OR_F16))
+        return OR_EINVAL;
+    int es = elem_size(dtype);
+    item_t *items = NULL;
+    const int64_t m = (n < k) ? n : k;  /* kept columns */
+    if (n > 0) {
+        items = (item_t *)malloc((size_t)n * sizeof(item_t));
+        if (!items)
+            return OR_ENOMEM;
+        for (int64_t j = 0; j < n; ++j) {
+            items[j].v = widen(row, dtype, j);
+            items[j].j = j;
+        }
+        qsort(items, (size_t)n, sizeof(item_t), by_value_desc_index_desc);
+        qsort(items, (size_t)m, sizeof(item_t), by_value_desc_index_asc);
+    }
+    for (int64_t s = 0; s < k; ++s) {
+        if (s < m) {
+            out_idx[s] = (int32_t)items[s].j;
+            if (out_val)
+                memcpy((char *)out_val + es * s, (const char *)row + es * items[s].j, es);
+        } else {
+            out_idx[s] = -1;
+            if (out_val)
+                write_pad_value(out_val, dtype, s);
+        }
+    }
+    free(items);
+    return OR_OK;
+}
+
+/* oracle_topk_varlen with a tie mode: tie_large = 0 keeps the smallest
+ * columns among ties, 1 the largest. */
+int oracle_topk_varlen_ties(const void *logits, int dtype, int64_t num_rows,
+                            int64_t width, int64_t row_stride,
+                            const int32_t *seq_lens, int32_t next_n,
+                            int32_t compress_ratio, int32_t k, int tie_large,
+                            int32_t *out_idx, void *out_val)
+{
+    if (num_rows < 0 || width < 0 || row_stride < width || next_n < 1 ||
+        compress_ratio < 1 || k < 1 || num_rows % next_n != 0)
+        return OR_EINVAL;
+    int es = elem_size(dtype);
+    for (int64_t r = 0; r < num_rows; ++r) {
+        int64_t n = oracle_row_length(seq_lens[r / next_n], next_n, r % next_n,
+                                      compress_ratio, width);
+        const char *row = (const char *)logits + (size_t)(r * row_stride) * es;
+        void *ov = out_val ? (char *)out_val + (size_t)(r * k) * es : NULL;
+        int rc = tie_large ? oracle_select_row_large_ties(row, dtype, n, k, out_idx + r * k, ov)
+                           : oracle_select_row(row, dtype, n, k, out_idx + r * k, ov);
+        if (rc != OR_OK)
+            return rc;
+    }
+    return OR_OK;
+}
+
 int oracle_topk_varlen(const void *logits, int dtype, int64_t num_rows,
                        int64_t width, int64_t row_stride,
                        const int32_t *seq_lens, int32_t next_n,

@@ -44,6 +44,8 @@ def _bind(lib):
     lib.oracle_ragged_offset_transform.restype = ctypes.c_int
     lib.oracle_ragged_offset_transform.argtypes = [
         vp, ctypes.c_int, i64, i64, i64, vp, vp, vp, i32, vp]
+    lib.oracle_select_row_large_ties.restype = ctypes.c_int
+    lib.oracle_select_row_large_ties.argtypes = [vp, ctypes.c_int, i64, i32, vp, vp]
     lib.oracle_seqs_page_table_transform.restype = ctypes.c_int
     lib.oracle_seqs_page_table_transform.argtypes = [
         vp, ctypes.c_int, i64, i64, i64, vp, vp, vp, i64, i64, vp, i64, i32, vp]
@@ -106,6 +108,14 @@ def golden_failures(lib):
             out.data_ptr(), raw.data_ptr())
         if rc != 0 or out.tolist() != case["out"] or raw.tolist() != case["out_raw"]:
             fails.append(f"page_table {case['name']}: rc={rc} {out.tolist()} {raw.tolist()}")
+    for case in _golden("ties.json")["cases"]:
+        row = torch.tensor(case["row"], dtype=torch.float32)
+        k = case["k"]
+        for mode, fn in (("small", lib.oracle_select_row), ("large", lib.oracle_select_row_large_ties)):
+            idx = torch.empty(k, dtype=torch.int32)
+            rc = fn(row.data_ptr(), 0, row.numel(), k, idx.data_ptr(), None)
+            if rc != 0 or idx.tolist() != case[mode]:
+                fails.append(f"ties {case['name']} {mode}: rc={rc} {idx.tolist()}")
     ep = _golden("epilogues.json")
     for case in ep["ragged"]:
         scores = torch.tensor([case["scores"]], dtype=torch.float32)
@@ -253,8 +263,10 @@ MUTANTS = [
     ("dropped +1 in numerator", "int64_t num = seq_len - next_n + t + 1;",
      "int64_t num = seq_len - next_n + t;"),
     ("missing width clamp", "return n < width ? n : width;", "return n;"),
-    ("ascending order", "if (x->v > y->v)\n        return -1;",
-     "if (x->v > y->v)\n        return 1;"),
+    ("ascending order", "if (x->v > y->v)\n        return -1;\n    if (x->v < y->v)\n        return 1;\n"
+                        "    return (x->j < y->j)",
+     "if (x->v > y->v)\n        return 1;\n    if (x->v < y->v)\n        return -1;\n"
+     "    return (x->j < y->j)"),
     ("tie order reversed", "return (x->j < y->j) ? -1 : (x->j > y->j ? 1 : 0);",
      "return (x->j > y->j) ? -1 : (x->j < y->j ? 1 : 0);"),
     ("page-table start dropped", "int64_t col = pt_start + idx / page_size;",
@@ -271,6 +283,9 @@ MUTANTS = [
     ("request row dropped", "page_table[b * pt_row_stride + idx]", "page_table[idx]"),
     ("request bounds off by one", "cu_seqlens_q[q] <= r && r < cu_seqlens_q[q + 1]",
      "cu_seqlens_q[q] <= r && r <= cu_seqlens_q[q + 1]"),
+    ("large ties keep the small columns", "return (x->j > y->j) ? -1 : (x->j < y->j ? 1 : 0);",
+     "return (x->j < y->j) ? -1 : (x->j > y->j ? 1 : 0);"),
+    ("large ties left unsorted", "        qsort(items, (size_t)m, sizeof(item_t), by_value_desc_index_asc);\n", ""),
 ]
 
 
@@ -323,3 +338,17 @@ def test_epilogue_variants_brute_force(oracle_mod):
         b = next((q for q in range(len(cu) - 1) if cu[q] <= r < cu[q + 1]), None)
         want = [-1] * k if b is None else [pt[b][i] if 0 <= i < 10 else -1 for i in local_topk(r)]
         assert out2[r].tolist() == want
+
+
+def test_large_ties_brute_force(oracle_mod):
+    """LARGE tie mode against pure Python on small alphabets (many ties)."""
+    rnd = random.Random(12)
+    for trial in range(200):
+        n = rnd.randint(0, 20)
+        k = rnd.randint(1, 24)
+        vals = [float(rnd.choice([-1, 0, 0, 1, 2, 2])) for _ in range(max(n, 1))]
+        row = torch.tensor(vals, dtype=torch.float32).view(1, -1)
+        idx, _ = oracle_mod.topk_varlen_ties(row, torch.tensor([n], dtype=torch.int32), k, True)
+        keep = sorted(range(n), key=lambda j: (-vals[j], -j))[:k]
+        want = sorted(keep, key=lambda j: (-vals[j], j)) + [-1] * (k - min(k, n))
+        assert idx[0].tolist() == want, (vals[:n], k)
