@@ -42,6 +42,15 @@ extern "C" {
 /* Largest supported top_k. */
 #define GBTOPK_MAX_TOP_K 2048
 
+/* Flags of the `deterministic` argument (FlashInfer compact page-table PR
+ * body, "SMALL/LARGE tie selection" and the deterministic output order).
+ * 0 asks for none: ties at the k-th value are resolved arbitrarily and the
+ * selected columns come in no particular order. */
+#define GBTOPK_SORTED 1     /* each row ordered by (value descending, column ascending);
+                               alone it implies GBTOPK_TIE_SMALL */
+#define GBTOPK_TIE_SMALL 2  /* among values equal to the k-th, keep the smallest columns */
+#define GBTOPK_TIE_LARGE 4  /* among values equal to the k-th, keep the largest columns */
+
 /*
  * gbtopk_varlen — top-K over decode-step indexer logits.
  *
@@ -74,11 +83,15 @@ extern "C" {
  *  out_values   device, dtype of logits, [num_rows, top_k], 16-byte aligned,
  *               or NULL.  Selected values are bit copies; padding slots hold
  *               the lowest finite value of the dtype.
- *  deterministic  0: ties at the k-th value are resolved arbitrarily and the
- *               selected columns come in no particular order.  1: ties take
- *               the smallest columns and each row is ordered by (value
- *               descending, column ascending).  Short rows (n_r <= top_k)
- *               come in column order when 0.
+ *  deterministic  0 or a set of GBTOPK_SORTED / GBTOPK_TIE_SMALL /
+ *               GBTOPK_TIE_LARGE (the two tie modes exclude each other;
+ *               other bits are GBTOPK_EINVAL).  0: ties at the k-th value
+ *               are resolved arbitrarily and the selected columns come in no
+ *               particular order.  1 (GBTOPK_SORTED): ties take the smallest
+ *               columns and each row is ordered by (value descending, column
+ *               ascending).  A tie mode fixes the selected set; without
+ *               GBTOPK_SORTED its order is unspecified.  Short rows
+ *               (n_r <= top_k) come in column order unless sorted.
  *  workspace    device scratch of at least gbtopk_workspace_bytes(...) bytes,
  *               256-byte aligned.  Its first 4 bytes are a status word that
  *               should start at zero (see gbtopk_device_status); everything

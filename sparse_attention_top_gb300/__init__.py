@@ -28,7 +28,7 @@ __all__ = [
     "gbtopk_plan_query", "gbtopk_status_str", "gbtopk_varlen_static_ws", "library_path",
     "load_library", "top_k_ragged_transform", "top_k_page_table_transform_cu_seqlens",
     "gbtopk_ragged_transform", "gbtopk_page_table_transform_cu_seqlens",
-    "GbtopkError", "MAX_TOP_K",
+    "GbtopkError", "MAX_TOP_K", "SORTED", "TIE_SMALL", "TIE_LARGE", "order_flags",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -39,6 +39,18 @@ _lock = threading.Lock()
 OK, HINT_DISCARDED = 0, 1
 EINVAL, EALIGN, EOVERLAP, EUNSUPPORTED, ECUDA, EWORKSPACE, ETIMEOUT = -1, -2, -3, -4, -5, -6, -7
 MAX_TOP_K = 2048
+# Flags of the C entry points' `deterministic` argument (include/gbtopk.h).
+SORTED, TIE_SMALL, TIE_LARGE = 1, 2, 4
+
+
+def order_flags(deterministic: bool = False, tie_mode: Optional[str] = None) -> int:
+    """Flags for ``deterministic`` and a tie mode among values equal to the
+    k-th: None (arbitrary, or the smallest columns when ``deterministic``),
+    "small" (smallest columns) or "large" (largest columns)."""
+    ties = {None: 0, "small": TIE_SMALL, "large": TIE_LARGE}
+    if tie_mode not in ties:
+        raise ValueError('tie_mode must be None, "small" or "large"')
+    return (SORTED if deterministic else 0) | ties[tie_mode]
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 
 
@@ -135,7 +147,7 @@ def gbtopk_device_status(workspace: torch.Tensor) -> int:
 def gbtopk_varlen(logits: torch.Tensor, seq_lens: torch.Tensor, top_k: int,
                   pre_idx: Optional[torch.Tensor], next_n: int, compress_ratio: int,
                   out_indices: torch.Tensor, out_values: Optional[torch.Tensor],
-                  deterministic: bool, workspace: torch.Tensor, stream=None) -> int:
+                  deterministic: int, workspace: torch.Tensor, stream=None) -> int:
     """Direct call of the C entry point on tensors (no checks beyond the library's)."""
     R, W = logits.shape
     stride = logits.stride(0) if R > 1 else W
@@ -143,14 +155,14 @@ def gbtopk_varlen(logits: torch.Tensor, seq_lens: torch.Tensor, top_k: int,
     return _check(load_library().gbtopk_varlen(
         _ptr(logits), _DTYPES[logits.dtype], R, W, stride, _ptr(seq_lens), next_n,
         compress_ratio, top_k, _ptr(pre_idx), _ptr(out_indices), _ptr(out_values),
-        1 if deterministic else 0, _ptr(workspace), workspace.numel() * workspace.element_size(),
+        int(deterministic), _ptr(workspace), workspace.numel() * workspace.element_size(),
         s))
 
 
 def gbtopk_varlen_static_ws(logits: torch.Tensor, seq_lens: torch.Tensor, top_k: int,
                             pre_idx: Optional[torch.Tensor], next_n: int, compress_ratio: int,
                             out_indices: torch.Tensor, out_values: Optional[torch.Tensor],
-                            deterministic: bool, stream=None) -> int:
+                            deterministic: int, stream=None) -> int:
     """Direct call of the allocation-free variant (library-owned 16 MiB scratch
     per GPU, shared by every call: serialise calls that could overlap)."""
     R, W = logits.shape
@@ -159,14 +171,14 @@ def gbtopk_varlen_static_ws(logits: torch.Tensor, seq_lens: torch.Tensor, top_k:
     return _check(load_library().gbtopk_varlen_static_ws(
         _ptr(logits), _DTYPES[logits.dtype], R, W, stride, _ptr(seq_lens), next_n,
         compress_ratio, top_k, _ptr(pre_idx), _ptr(out_indices), _ptr(out_values),
-        1 if deterministic else 0, s))
+        int(deterministic), s))
 
 
 def gbtopk_page_table_transform(scores: torch.Tensor, lengths: torch.Tensor,
                                 row_starts: Optional[torch.Tensor], page_table: torch.Tensor,
                                 page_table_row_starts: Optional[torch.Tensor], page_size: int,
                                 top_k: int, out: torch.Tensor, out_raw: Optional[torch.Tensor],
-                                deterministic: bool, workspace: torch.Tensor, stream=None) -> int:
+                                deterministic: int, workspace: torch.Tensor, stream=None) -> int:
     """Direct call of the C entry point on tensors."""
     R, W = scores.shape
     stride = scores.stride(0) if R > 1 else W
@@ -176,13 +188,13 @@ def gbtopk_page_table_transform(scores: torch.Tensor, lengths: torch.Tensor,
     return _check(load_library().gbtopk_page_table_transform(
         _ptr(scores), _DTYPES[scores.dtype], R, W, stride, _ptr(lengths), _ptr(row_starts),
         _ptr(page_table), P, pstride, _ptr(page_table_row_starts), page_size, top_k, _ptr(out),
-        _ptr(out_raw), 1 if deterministic else 0, _ptr(workspace),
+        _ptr(out_raw), int(deterministic), _ptr(workspace),
         workspace.numel() * workspace.element_size(), s))
 
 
 def gbtopk_ragged_transform(scores: torch.Tensor, lengths: torch.Tensor,
                             row_starts: Optional[torch.Tensor], topk_indices_offset: torch.Tensor,
-                            top_k: int, out: torch.Tensor, deterministic: bool,
+                            top_k: int, out: torch.Tensor, deterministic: int,
                             workspace: torch.Tensor, stream=None) -> int:
     """Direct call of the C entry point on tensors."""
     R, W = scores.shape
@@ -190,14 +202,14 @@ def gbtopk_ragged_transform(scores: torch.Tensor, lengths: torch.Tensor,
     s = _stream_handle(scores.device) if stream is None else stream
     return _check(load_library().gbtopk_ragged_transform(
         _ptr(scores), _DTYPES[scores.dtype], R, W, stride, _ptr(lengths), _ptr(row_starts),
-        _ptr(topk_indices_offset), top_k, _ptr(out), 1 if deterministic else 0, _ptr(workspace),
+        _ptr(topk_indices_offset), top_k, _ptr(out), int(deterministic), _ptr(workspace),
         workspace.numel() * workspace.element_size(), s))
 
 
 def gbtopk_page_table_transform_cu_seqlens(scores: torch.Tensor, lengths: torch.Tensor,
                                            row_starts: Optional[torch.Tensor],
                                            page_table: torch.Tensor, cu_seqlens_q: torch.Tensor,
-                                           top_k: int, out: torch.Tensor, deterministic: bool,
+                                           top_k: int, out: torch.Tensor, deterministic: int,
                                            workspace: torch.Tensor, stream=None) -> int:
     """Direct call of the C entry point on tensors."""
     R, W = scores.shape
@@ -208,7 +220,7 @@ def gbtopk_page_table_transform_cu_seqlens(scores: torch.Tensor, lengths: torch.
     return _check(load_library().gbtopk_page_table_transform_cu_seqlens(
         _ptr(scores), _DTYPES[scores.dtype], R, W, stride, _ptr(lengths), _ptr(row_starts),
         _ptr(page_table), P, pstride, _ptr(cu_seqlens_q), cu_seqlens_q.numel() - 1, top_k,
-        _ptr(out), 1 if deterministic else 0, _ptr(workspace),
+        _ptr(out), int(deterministic), _ptr(workspace),
         workspace.numel() * workspace.element_size(), s))
 
 
@@ -253,14 +265,18 @@ def top_k_varlen(logits: torch.Tensor, seq_lens: torch.Tensor, top_k: int,
                  next_n: int = 1, return_values: bool = False,
                  out_indices: Optional[torch.Tensor] = None,
                  out_values: Optional[torch.Tensor] = None, deterministic: bool = False,
-                 workspace: Optional[torch.Tensor] = None
+                 workspace: Optional[torch.Tensor] = None, tie_mode: Optional[str] = None
                  ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Top-k of each row of ``logits`` over its valid columns.
 
     Row t of request i ranks its first
     ``max(0, (seq_lens[i] - next_n + t + 1) // compress_ratio)`` columns,
     clamped to the width.  Returns ``(indices int32 [R, k], values | None)``;
-    unused slots are -1 (values: the dtype's lowest finite value)."""
+    unused slots are -1 (values: the dtype's lowest finite value).
+    ``deterministic`` orders each row by (value desc, column asc);
+    ``tie_mode`` ("small" / "large") fixes which columns equal to the k-th
+    value are kept (see ``order_flags``)."""
+    flags = order_flags(deterministic, tie_mode)
     _require_cuda(logits, "logits")
     _require_cuda(seq_lens, "seq_lens")
     if logits.dim() != 2 or logits.stride(1) != 1 or logits.dtype not in _DTYPES:
@@ -288,7 +304,7 @@ def top_k_varlen(logits: torch.Tensor, seq_lens: torch.Tensor, top_k: int,
     ws = workspace if workspace is not None else _workspace(
         logits.device, gbtopk_workspace_bytes(R, W, top_k, logits.dtype))
     st = gbtopk_varlen(logits, seq_lens, top_k, hint, next_n, compress_ratio, idx, val,
-                       deterministic, ws)
+                       flags, ws)
     if st == HINT_DISCARDED:
         warnings.warn("pre_idx is not 16-byte aligned and was discarded; running hint-free",
                       RuntimeWarning, stacklevel=2)
@@ -302,11 +318,14 @@ def top_k_page_table_transform(scores: torch.Tensor, lengths: torch.Tensor,
                                out: Optional[torch.Tensor] = None,
                                out_raw_indices: Optional[torch.Tensor] = None,
                                deterministic: bool = False,
-                               workspace: Optional[torch.Tensor] = None):
+                               workspace: Optional[torch.Tensor] = None,
+                               tie_mode: Optional[str] = None):
     """Top-k fused with the compact page-table transform.
 
     Returns ``out`` (physical indices), or ``(out, out_raw_indices)`` when a
-    raw-index buffer is given."""
+    raw-index buffer is given.  ``deterministic`` / ``tie_mode``: as for
+    ``top_k_varlen``."""
+    flags = order_flags(deterministic, tie_mode)
     for t, name in ((scores, "scores"), (lengths, "lengths"), (page_table, "page_table")):
         _require_cuda(t, name)
     if scores.dim() != 2 or scores.stride(1) != 1 or scores.dtype not in _DTYPES:
@@ -331,7 +350,7 @@ def top_k_page_table_transform(scores: torch.Tensor, lengths: torch.Tensor,
     ws = workspace if workspace is not None else _workspace(
         scores.device, gbtopk_workspace_bytes(R, W, top_k, scores.dtype))
     gbtopk_page_table_transform(scores, lengths, row_starts, page_table, page_table_row_starts,
-                                page_size, top_k, o, raw, deterministic, ws)
+                                page_size, top_k, o, raw, flags, ws)
     return (o, raw) if raw is not None else o
 
 
@@ -350,9 +369,11 @@ def top_k_ragged_transform(scores: torch.Tensor, lengths: torch.Tensor,
                            topk_indices_offset: torch.Tensor, top_k: int,
                            row_starts: Optional[torch.Tensor] = None,
                            out: Optional[torch.Tensor] = None, deterministic: bool = False,
-                           workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+                           workspace: Optional[torch.Tensor] = None,
+                           tie_mode: Optional[str] = None) -> torch.Tensor:
     """Top-k fused with the ragged KV index offset (SGLang
     fast_topk_transform_ragged_fused): out = idx + topk_indices_offset[row]."""
+    flags = order_flags(deterministic, tie_mode)
     _ragged_inputs(scores, lengths, row_starts,
                    ((scores, "scores"), (lengths, "lengths"),
                     (topk_indices_offset, "topk_indices_offset")))
@@ -364,7 +385,7 @@ def top_k_ragged_transform(scores: torch.Tensor, lengths: torch.Tensor,
     ws = workspace if workspace is not None else _workspace(
         scores.device, gbtopk_workspace_bytes(R, W, top_k, scores.dtype))
     gbtopk_ragged_transform(scores, lengths, row_starts, topk_indices_offset, top_k, o,
-                            deterministic, ws)
+                            flags, ws)
     return o
 
 
@@ -373,10 +394,12 @@ def top_k_page_table_transform_cu_seqlens(scores: torch.Tensor, lengths: torch.T
                                           top_k: int, row_starts: Optional[torch.Tensor] = None,
                                           out: Optional[torch.Tensor] = None,
                                           deterministic: bool = False,
-                                          workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+                                          workspace: Optional[torch.Tensor] = None,
+                                          tie_mode: Optional[str] = None) -> torch.Tensor:
     """Top-k fused with a page_size-1 page table indexed by request (SGLang
     fast_topk_transform_fused): row r of request b (cu_seqlens_q[b] <= r <
     cu_seqlens_q[b + 1]) gets page_table[b, idx]."""
+    flags = order_flags(deterministic, tie_mode)
     _ragged_inputs(scores, lengths, row_starts,
                    ((scores, "scores"), (lengths, "lengths"), (page_table, "page_table"),
                     (cu_seqlens_q, "cu_seqlens_q")))
@@ -390,5 +413,5 @@ def top_k_page_table_transform_cu_seqlens(scores: torch.Tensor, lengths: torch.T
     ws = workspace if workspace is not None else _workspace(
         scores.device, gbtopk_workspace_bytes(R, W, top_k, scores.dtype))
     gbtopk_page_table_transform_cu_seqlens(scores, lengths, row_starts, page_table, cu_seqlens_q,
-                                           top_k, o, deterministic, ws)
+                                           top_k, o, flags, ws)
     return o

@@ -102,9 +102,14 @@ using gbtopk::Plan;
 
 namespace {
 
+// `deterministic` is a set of GBTOPK_SORTED / GBTOPK_TIE_SMALL /
+// GBTOPK_TIE_LARGE flags; the two tie modes exclude each other.
 int check_common(const void *x, int dtype, int64_t num_rows, int64_t width, int64_t row_stride,
-                 int32_t top_k, const void *out, const void *workspace, size_t workspace_bytes,
-                 Plan *plan) {
+                 int32_t top_k, const void *out, int deterministic, const void *workspace,
+                 size_t workspace_bytes, Plan *plan) {
+    const int all = GBTOPK_SORTED | GBTOPK_TIE_SMALL | GBTOPK_TIE_LARGE;
+    if ((deterministic & ~all) != 0 || ((deterministic & GBTOPK_TIE_SMALL) && (deterministic & GBTOPK_TIE_LARGE)))
+        return GBTOPK_EINVAL;
     const int rc = gbtopk::make_plan(num_rows, width, top_k, dtype, plan);
     if (rc != GBTOPK_OK) return rc;
     if (num_rows == 0) return GBTOPK_OK;
@@ -135,8 +140,8 @@ int gbtopk_varlen(const void *logits, int dtype, int64_t num_rows, int64_t width
     if (next_n < 1 || compress_ratio < 1 || num_rows < 0 || num_rows % next_n != 0)
         return GBTOPK_EINVAL;
     Plan plan;
-    int rc = check_common(logits, dtype, num_rows, width, row_stride, top_k, out_indices, workspace,
-                          workspace_bytes, &plan);
+    int rc = check_common(logits, dtype, num_rows, width, row_stride, top_k, out_indices, deterministic,
+                          workspace, workspace_bytes, &plan);
     if (rc != GBTOPK_OK || num_rows == 0) return rc;
     if (!seq_lens) return GBTOPK_EINVAL;
     const size_t nout = static_cast<size_t>(num_rows) * static_cast<size_t>(top_k);
@@ -160,7 +165,7 @@ int gbtopk_varlen(const void *logits, int dtype, int64_t num_rows, int64_t width
     p.compress_ratio = compress_ratio;
     p.pre_idx = pre_idx;
     p.k = top_k;
-    p.deterministic = deterministic ? 1 : 0;
+    p.deterministic = deterministic;
     p.out_idx = out_indices;
     p.out_val = out_values;
     p.ws = static_cast<uint8_t *>(workspace);
@@ -175,8 +180,8 @@ int gbtopk_ragged_transform(const void *scores, int dtype, int64_t num_rows, int
                             int deterministic, void *workspace, size_t workspace_bytes, void *stream) {
     if (num_rows < 0) return GBTOPK_EINVAL;
     Plan plan;
-    int rc = check_common(scores, dtype, num_rows, width, row_stride, top_k, out, workspace,
-                          workspace_bytes, &plan);
+    int rc = check_common(scores, dtype, num_rows, width, row_stride, top_k, out, deterministic,
+                          workspace, workspace_bytes, &plan);
     if (rc != GBTOPK_OK || num_rows == 0) return rc;
     if (!lengths || !topk_indices_offset) return GBTOPK_EINVAL;
     Params p{};
@@ -189,7 +194,7 @@ int gbtopk_ragged_transform(const void *scores, int dtype, int64_t num_rows, int
     p.lengths = lengths;
     p.row_starts = row_starts;
     p.k = top_k;
-    p.deterministic = deterministic ? 1 : 0;
+    p.deterministic = deterministic;
     p.out_idx = out;
     p.idx_offset = topk_indices_offset;
     p.page_size = 1;
@@ -208,8 +213,8 @@ int gbtopk_page_table_transform_cu_seqlens(const void *scores, int dtype, int64_
     if (num_rows < 0 || num_reqs < 0 || pt_cols < 0) return GBTOPK_EINVAL;
     if (num_reqs > 1 && pt_row_stride < pt_cols) return GBTOPK_EINVAL;
     Plan plan;
-    int rc = check_common(scores, dtype, num_rows, width, row_stride, top_k, out, workspace,
-                          workspace_bytes, &plan);
+    int rc = check_common(scores, dtype, num_rows, width, row_stride, top_k, out, deterministic,
+                          workspace, workspace_bytes, &plan);
     if (rc != GBTOPK_OK || num_rows == 0) return rc;
     if (!lengths || !page_table || !cu_seqlens_q) return GBTOPK_EINVAL;
     Params p{};
@@ -222,7 +227,7 @@ int gbtopk_page_table_transform_cu_seqlens(const void *scores, int dtype, int64_
     p.lengths = lengths;
     p.row_starts = row_starts;
     p.k = top_k;
-    p.deterministic = deterministic ? 1 : 0;
+    p.deterministic = deterministic;
     p.out_idx = out;
     p.page_table = page_table;
     p.pt_cols = pt_cols;
@@ -246,8 +251,8 @@ int gbtopk_page_table_transform(const void *scores, int dtype, int64_t num_rows,
     if (num_rows > 1 && pt_row_stride < pt_cols) return GBTOPK_EINVAL;
     if (page_size > 1 && row_starts && !pt_row_starts) return GBTOPK_EINVAL;
     Plan plan;
-    int rc = check_common(scores, dtype, num_rows, width, row_stride, top_k, out, workspace,
-                          workspace_bytes, &plan);
+    int rc = check_common(scores, dtype, num_rows, width, row_stride, top_k, out, deterministic,
+                          workspace, workspace_bytes, &plan);
     if (rc != GBTOPK_OK || num_rows == 0) return rc;
     if (!lengths || !page_table) return GBTOPK_EINVAL;
     const size_t nout = static_cast<size_t>(num_rows) * static_cast<size_t>(top_k) * 4;
@@ -265,7 +270,7 @@ int gbtopk_page_table_transform(const void *scores, int dtype, int64_t num_rows,
     p.lengths = lengths;
     p.row_starts = row_starts;
     p.k = top_k;
-    p.deterministic = deterministic ? 1 : 0;
+    p.deterministic = deterministic;
     p.out_idx = out;
     p.out_raw = out_raw;
     p.page_table = page_table;

@@ -32,6 +32,18 @@ constexpr size_t kWsHeaderBytes = 256; // device status word + padding
 constexpr size_t kRowInfoBytes = 16;   // t_lo, bin shift (written by the row kernel)
 constexpr uint32_t kSpinLimit = 1u << 22;
 
+// Flags of Params::deterministic (the public GBTOPK_SORTED / GBTOPK_TIE_*).
+constexpr int kSortedFlag = 1;
+constexpr int kTieSmallFlag = 2;
+constexpr int kTieLargeFlag = 4;
+
+// Tie mode among values equal to the k-th: 0 any, 1 smallest columns (also
+// implied by the sorted flag alone), 2 largest columns.
+__host__ __device__ inline int tie_mode(int flags) {
+    return (flags & kTieLargeFlag) ? 2 : ((flags & (kSortedFlag | kTieSmallFlag)) ? 1 : 0);
+}
+__host__ __device__ inline bool sorted_output(int flags) { return (flags & kSortedFlag) != 0; }
+
 // Bits of the device status word.
 constexpr uint32_t kStatusWaitTimeout = 1u;
 
@@ -61,7 +73,7 @@ struct Params {
     const int32_t *row_starts;
     const int32_t *pre_idx;
     int32_t k;
-    int32_t deterministic;
+    int32_t deterministic;       // kSortedFlag | kTieSmallFlag | kTieLargeFlag
     int32_t *out_idx;
     void *out_val;
     int32_t *out_raw;

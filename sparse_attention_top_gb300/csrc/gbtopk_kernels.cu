@@ -341,10 +341,15 @@ struct RankByKey {
     }
 };
 
+// Tie modes (among values equal to the k-th): 0 any, 1 the smallest
+// columns, 2 the largest.  tie_key orders the preferred columns first.
+__device__ __forceinline__ uint32_t tie_key(uint32_t col, int tie) { return tie == 2 ? ~col : col; }
+
 struct RankTieColumn {
     uint32_t t;
+    int tie;
     __device__ __forceinline__ bool operator()(uint32_t key, uint32_t idx, uint32_t &k) const {
-        k = ~idx;
+        k = ~tie_key(idx, tie);
         return key == t;
     }
 };
@@ -417,11 +422,11 @@ __device__ void block_select(const Src &src, const Mode &mode, int64_t cnt, uint
 }
 
 // Writes every item with key > t into sel[base + 0 ..) and `need_ties`
-// items with key == t into sel[base + gt ..).  Deterministic mode keeps the
-// ties whose column is <= tie_col_max (exactly need_ties of them).
+// items with key == t into sel[base + gt ..).  With a tie mode it keeps the
+// ties whose tie_key is <= tie_col_max (exactly need_ties of them).
 template <int DT, class S>
 __device__ void collect(const S &s, int64_t cnt, uint32_t t, uint32_t gt, uint32_t need_ties,
-                        bool det, uint32_t tie_col_max, uint2 *sel, uint32_t base, Ctrl &c) {
+                        int tie, uint32_t tie_col_max, uint2 *sel, uint32_t base, Ctrl &c) {
     if (threadIdx.x == 0) {
         c.sel_count = 0;
         c.tie_count = 0;
@@ -429,30 +434,30 @@ __device__ void collect(const S &s, int64_t cnt, uint32_t t, uint32_t gt, uint32
     __syncthreads();
     for_each_item(s, cnt, [&](bool valid, uint32_t key, uint32_t idx, uint32_t raw) {
         const bool above = valid && key > t;
-        const bool tie = valid && key == t && (!det || idx <= tie_col_max);
+        const bool keep = valid && key == t && (!tie || tie_key(idx, tie) <= tie_col_max);
         const uint32_t slot = warp_claim(&c.sel_count, above);
         if (above) sel[base + slot] = make_uint2(raw, idx);
-        const uint32_t tslot = warp_claim(&c.tie_count, tie);
-        if (tie && tslot < need_ties) sel[base + gt + tslot] = make_uint2(raw, idx);
+        const uint32_t tslot = warp_claim(&c.tie_count, keep);
+        if (keep && tslot < need_ties) sel[base + gt + tslot] = make_uint2(raw, idx);
     });
     __syncthreads();
 }
 
 // Exact top-k (n > k) of a source into sel[0..k).
 template <int DT, class S>
-__device__ void exact_select(const S &s, int64_t n, int k, bool det, uint2 *sel, uint32_t *hist,
+__device__ void exact_select(const S &s, int64_t n, int k, int tie, uint2 *sel, uint32_t *hist,
                              Ctrl &c) {
     constexpr int KB = Elem<DT>::kKeyBits;
     uint32_t t, gt;
     block_select<KB, KB / 8>(s, RankByKey{}, n, static_cast<uint32_t>(k), hist, c, t, gt);
     const uint32_t need_ties = static_cast<uint32_t>(k) - gt;
     uint32_t col_max = 0xFFFFFFFFu;
-    if (det) {
+    if (tie) {
         uint32_t kk, g2;
-        block_select<32, 4>(s, RankTieColumn{t}, n, need_ties, hist, c, kk, g2);
+        block_select<32, 4>(s, RankTieColumn{t, tie}, n, need_ties, hist, c, kk, g2);
         col_max = ~kk;
     }
-    collect<DT>(s, n, t, gt, need_ties, det, col_max, sel, 0, c);
+    collect<DT>(s, n, t, gt, need_ties, tie, col_max, sel, 0, c);
 }
 
 // ---------------------------------------------------------------- row geometry and output
@@ -894,7 +899,7 @@ __device__ uint32_t filter_staged(const void *stage, int off, int len, int col_b
 // `sel` may alias `hist` (the histogram is consumed first).
 template <int DT, int NT, class CandSrc>
 __device__ bool select_from_candidates(const CandSrc &cands, uint32_t total, const uint32_t *hist,
-                                       uint32_t t_lo, int bin_shift, int k, bool det, uint2 *sel,
+                                       uint32_t t_lo, int bin_shift, int k, int tie, uint2 *sel,
                                        uint2 *blist, uint32_t bcap, Ctrl &c) {
     constexpr int KB = Elem<DT>::kKeyBits;
     find_bin_from_top<NT>(hist, static_cast<uint32_t>(k), c);
@@ -926,7 +931,7 @@ __device__ bool select_from_candidates(const CandSrc &cands, uint32_t total, con
             for (uint32_t j = 0; j < bsize; ++j) {
                 const uint2 o = blist[j];
                 const uint32_t ok = Elem<DT>::key(o.x);
-                rank += (ok > mk || (ok == mk && o.y < me.y)) ? 1u : 0u;
+                rank += (ok > mk || (ok == mk && tie_key(o.y, tie) < tie_key(me.y, tie))) ? 1u : 0u;
             }
             if (rank < need) sel[above + rank] = me;
         }
@@ -937,12 +942,12 @@ __device__ bool select_from_candidates(const CandSrc &cands, uint32_t total, con
         block_select<KB, KB / 8>(bs, RankByKey{}, bsize, need, c.rhist, c, t, gt);
         const uint32_t need_ties = need - gt;
         uint32_t col_max = 0xFFFFFFFFu;
-        if (det) {
+        if (tie) {
             uint32_t kk, g2;
-            block_select<32, 4>(bs, RankTieColumn{t}, bsize, need_ties, c.rhist, c, kk, g2);
+            block_select<32, 4>(bs, RankTieColumn{t, tie}, bsize, need_ties, c.rhist, c, kk, g2);
             col_max = ~kk;
         }
-        collect<DT>(bs, bsize, t, gt, need_ties, det, col_max, sel, above, c);
+        collect<DT>(bs, bsize, t, gt, need_ties, tie, col_max, sel, above, c);
     }
     return true;
 }
@@ -989,7 +994,8 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
     const uint32_t stage_pairs = static_cast<uint32_t>((p.plan.row_smem - p.plan.off_stage) / sizeof(uint2));
     const int64_t row = p.row0 + blockIdx.x;
     const int k = p.k;
-    const bool det = p.deterministic != 0;
+    const bool sorted = sorted_output(p.deterministic);
+    const int tie = tie_mode(p.deterministic);
     constexpr int kTraceBase = 0;
     (void)kTraceBase;
 
@@ -1086,11 +1092,11 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
 
     // ---- short and empty rows: every valid column, then -1
     if (n <= k) {
-        const bool need_raw = det || p.out_val != nullptr;
+        const bool need_raw = sorted || p.out_val != nullptr;
         for (int j = threadIdx.x; j < n; j += blockDim.x)
             sel[j] = make_uint2(need_raw ? ldg_raw(xrow + j) : 0u, static_cast<uint32_t>(j));
         __syncthreads();
-        if (det) emit_sorted<DT>(p, row, sel, static_cast<int>(n), smem + p.plan.row_smem, c);
+        if (sorted) emit_sorted<DT>(p, row, sel, static_cast<int>(n), smem + p.plan.row_smem, c);
         else emit<DT>(p, row, sel, static_cast<int>(n));
         GBTOPK_TRACE_POINT(6, 0);
         GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | 1u);
@@ -1137,10 +1143,10 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
         __syncthreads();
         if (total >= static_cast<uint32_t>(k) && total <= stage_pairs)
             done = select_from_candidates<DT, kThreads>(PairSrc<DT>{lcand}, total, hist, t_lo, bin_shift,
-                                                        k, det, sel, lcand + total, stage_pairs - total, c);
+                                                        k, tie, sel, lcand + total, stage_pairs - total, c);
     }
-    if (!done) exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, det, sel, c.rhist, c);
-    if (det) emit_sorted<DT>(p, row, sel, k, smem + p.plan.row_smem, c);
+    if (!done) exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, tie, sel, c.rhist, c);
+    if (sorted) emit_sorted<DT>(p, row, sel, k, smem + p.plan.row_smem, c);
     else emit<DT>(p, row, sel, k);
     if (!ok && threadIdx.x == 0) mbar_wait(&c.bar, 0);  // let the copy land before exit
     GBTOPK_TRACE_POINT(6, 0);
@@ -1443,7 +1449,7 @@ constexpr uint32_t kPadColumn = 0xFFFFFFFFu;  // marks a gather padding slot
 // Completes sel[above, above + need) with the best `need` of the bsize
 // members of the boundary bin (blist), ranked by (key desc, column asc).
 template <int DT, int NT>
-__device__ bool rank_boundary(const uint2 *blist, uint32_t bsize, uint32_t need, uint32_t above, bool det,
+__device__ bool rank_boundary(const uint2 *blist, uint32_t bsize, uint32_t need, uint32_t above, int tie,
                               uint2 *sel, Ctrl &c) {
     const uint32_t tid = threadIdx.x;
     if (bsize <= kRankMax) {
@@ -1456,7 +1462,7 @@ __device__ bool rank_boundary(const uint2 *blist, uint32_t bsize, uint32_t need,
             for (uint32_t j2 = lane; j2 < bsize; j2 += 32) {
                 const uint2 o = blist[j2];
                 const uint32_t ok = Elem<DT>::key(o.x);
-                rank += (ok > mk || (ok == mk && o.y < me.y)) ? 1u : 0u;
+                rank += (ok > mk || (ok == mk && tie_key(o.y, tie) < tie_key(me.y, tie))) ? 1u : 0u;
             }
             rank = __reduce_add_sync(0xffffffffu, rank);
             if (lane == 0 && rank < need) sel[above + rank] = me;
@@ -1469,12 +1475,12 @@ __device__ bool rank_boundary(const uint2 *blist, uint32_t bsize, uint32_t need,
         block_select<KB, KB / 8>(bs, RankByKey{}, bsize, need, c.rhist, c, t, gt);
         const uint32_t need_ties = need - gt;
         uint32_t col_max = 0xFFFFFFFFu;
-        if (det) {
+        if (tie) {
             uint32_t kk, g2;
-            block_select<32, 4>(bs, RankTieColumn{t}, bsize, need_ties, c.rhist, c, kk, g2);
+            block_select<32, 4>(bs, RankTieColumn{t, tie}, bsize, need_ties, c.rhist, c, kk, g2);
             col_max = ~kk;
         }
-        collect<DT>(bs, bsize, t, gt, need_ties, det, col_max, sel, above, c);
+        collect<DT>(bs, bsize, t, gt, need_ties, tie, col_max, sel, above, c);
     }
     return true;
 }
@@ -1490,7 +1496,7 @@ __device__ bool rank_boundary(const uint2 *blist, uint32_t bsize, uint32_t need,
 // kFinalBCap members.
 template <int DT, int NT>
 __device__ bool select_gathered(const uint2 *cand, uint32_t total_p, uint32_t t_lo, int bin_shift, int k,
-                                bool det, uint32_t *hist, uint2 *sel, uint2 *blist, Ctrl &c) {
+                                int tie, uint32_t *hist, uint2 *sel, uint2 *blist, Ctrl &c) {
     const uint32_t tid = threadIdx.x;
 #pragma unroll
     for (int j = 0; j < kBins / NT; ++j) hist[tid + j * NT] = 0;
@@ -1528,7 +1534,7 @@ __device__ bool select_gathered(const uint2 *cand, uint32_t total_p, uint32_t t_
         else if (b == bstar) blist[es++] = v;
     }
     __syncthreads();
-    return rank_boundary<DT, NT>(blist, bsize, static_cast<uint32_t>(k) - above, above, det, sel, c);
+    return rank_boundary<DT, NT>(blist, bsize, static_cast<uint32_t>(k) - above, above, tie, sel, c);
 }
 
 // Exact top-k among `total` (>= k) candidates left in workspace segments
@@ -1539,7 +1545,7 @@ __device__ bool select_gathered(const uint2 *cand, uint32_t total_p, uint32_t t_
 // contract as select_gathered.
 template <int DT, int NT>
 __device__ bool select_from_segments(const SegMap &map, uint32_t total, uint32_t t_lo, int bin_shift, int k,
-                                     bool det, uint32_t *hist, uint2 *sel, uint2 *blist, Ctrl &c) {
+                                     int tie, uint32_t *hist, uint2 *sel, uint2 *blist, Ctrl &c) {
     constexpr int GB = 8;  // candidates in flight per thread
     const uint32_t tid = threadIdx.x;
 #pragma unroll
@@ -1599,7 +1605,7 @@ __device__ bool select_from_segments(const SegMap &map, uint32_t total, uint32_t
         eq_base += ptot & 0xFFFFu;
     }
     __syncthreads();
-    return rank_boundary<DT, NT>(blist, bsize, static_cast<uint32_t>(k) - above, above, det, sel, c);
+    return rank_boundary<DT, NT>(blist, bsize, static_cast<uint32_t>(k) - above, above, tie, sel, c);
 }
 
 template <int DT>
@@ -1618,7 +1624,8 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
                               4 * static_cast<size_t>(kFinalThreads))) / sizeof(uint2));
     const int64_t row = p.row0 + blockIdx.x;
     const int k = p.k;
-    const bool det = p.deterministic != 0;
+    const bool sorted = sorted_output(p.deterministic);
+    const int tie = tie_mode(p.deterministic);
     const int tid = threadIdx.x;
     constexpr int kTraceBase = 40960;
     (void)kTraceBase;
@@ -1672,7 +1679,7 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
             if (tid < nch && (cnt & 1u)) cand[poff + cnt].y = kPadColumn;
             __syncthreads();
             GBTOPK_TRACE_POINT(1, 0);
-            if (!select_gathered<DT, kFinalThreads>(cand, total_p, t_lo, bin_shift, k, det, hist, sel, blist, c))
+            if (!select_gathered<DT, kFinalThreads>(cand, total_p, t_lo, bin_shift, k, tie, hist, sel, blist, c))
                 fallback = true;
         } else {
             fallback = true;
@@ -1683,16 +1690,16 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
         if (tid < nch) choff[tid] = base;
         __syncthreads();
         if (!select_from_segments<DT, kFinalThreads>(SegMap{segs, choff, static_cast<int>(nch), cap}, total, t_lo,
-                                                     bin_shift, k, det, hist, sel, blist, c))
+                                                     bin_shift, k, tie, hist, sel, blist, c))
             fallback = true;
     }
-    if (fallback) exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, det, sel, c.rhist, c);
+    if (fallback) exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, tie, sel, c.rhist, c);
     GBTOPK_TRACE_POINT(2, 0);
     // the next call's first kernel may launch now (it waits for this grid
     // to complete before reading anything)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (!copy_ok && tid == 0) mbar_wait(&c.bar, 0);  // let the copies land (before reusing cand)
-    if (det) {
+    if (sorted) {
         __syncthreads();
         emit_sorted<DT>(p, row, sel, k, reinterpret_cast<uint8_t *>(cand), c);
     } else {
@@ -1705,14 +1712,14 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
 
 // ---------------------------------------------------------------- small rows
 
-// Small-row kernel (widths up to 32 * NE <= 2048 columns, non-deterministic
-// calls): one warp per row, no block barrier.  Lane l holds columns l,
-// l + 32, ..., as keys in registers.  The k-th largest key t comes from a
-// radix select over 8-bit digits with a warp-private 256-bin shared
-// histogram (two rounds for 16-bit keys, four for fp32).  The keys above t
-// and the first k - #(keys > t) keys equal to t in column order are then
-// written in column order, each warp-wide slot from two ballots per
-// register.
+// Small-row kernel (widths up to 32 * NE <= 2048 columns, calls without the
+// sorted output order): one warp per row, no block barrier.  Lane l holds
+// columns l, l + 32, ..., as keys in registers.  The k-th largest key t
+// comes from a radix select over 8-bit digits with a warp-private 256-bin
+// shared histogram (two rounds for 16-bit keys, four for fp32).  The keys
+// above t and k - #(keys > t) keys equal to t (the first in column order,
+// or the last with the largest-columns tie mode) are then written in column
+// order, each warp-wide slot from two ballots per register.
 template <int DT, int NE>
 __global__ void __launch_bounds__(128) small_kernel(const __grid_constant__ Params p) {
     using raw_t = typename Elem<DT>::raw_t;
@@ -1744,7 +1751,7 @@ __global__ void __launch_bounds__(128) small_kernel(const __grid_constant__ Para
         // one 256-bin shared histogram per warp (columns past the row hold
         // key 0, which no real value maps to, and are left out)
         uint32_t *h = small_hist + (threadIdx.x >> 5) * 256;
-        uint32_t prefix = 0, pmask = 0, rem = static_cast<uint32_t>(k);
+        uint32_t prefix = 0, pmask = 0, rem = static_cast<uint32_t>(k), bin_n = 0;
 #pragma unroll 1
         for (int shift = KB - 8; shift >= 0; shift -= 8) {
 #pragma unroll
@@ -1768,17 +1775,19 @@ __global__ void __launch_bounds__(128) small_kernel(const __grid_constant__ Para
             }
             const uint32_t excl = incl - sum;
             const uint32_t owner = __ffs(__ballot_sync(0xffffffffu, excl < rem && rem <= incl)) - 1;
-            uint32_t digit = 0, above = excl;
+            uint32_t digit = 0, above = excl, nd = 0;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 if (above + cnt[j] >= rem) {
                     digit = 255u - 8u * lane - static_cast<uint32_t>(j);
+                    nd = cnt[j];
                     break;
                 }
                 above += cnt[j];
             }
             digit = __shfl_sync(0xffffffffu, digit, owner);
             above = __shfl_sync(0xffffffffu, above, owner);
+            bin_n = __shfl_sync(0xffffffffu, nd, owner);  // after the last digit: #(keys == t)
             prefix |= digit << shift;
             pmask |= 255u << shift;
             rem -= above;
@@ -1786,7 +1795,10 @@ __global__ void __launch_bounds__(128) small_kernel(const __grid_constant__ Para
         }
         const uint32_t t = prefix;
         const uint32_t gt = static_cast<uint32_t>(k) - rem;
-        const uint32_t need = rem;  // ties taken, smallest columns first
+        // ties taken: the first `need` in column order, or with the
+        // largest-columns tie mode the last `need` (the first `skip` are passed over)
+        const uint32_t need = rem;
+        const uint32_t skip = tie_mode(p.deterministic) == 2 ? bin_n - need : 0u;
         const uint32_t lt = lanemask_lt();
         uint32_t hi_base = 0, tie_base = 0;
 #pragma unroll
@@ -1794,7 +1806,7 @@ __global__ void __launch_bounds__(128) small_kernel(const __grid_constant__ Para
             const bool h = key[e] > t, q = key[e] == t;
             const uint32_t bh = __ballot_sync(0xffffffffu, h);
             const uint32_t bt = __ballot_sync(0xffffffffu, q);
-            const uint32_t r = tie_base + __popc(bt & lt);
+            const uint32_t r = tie_base + __popc(bt & lt) - skip;  // wraps for passed-over ties
             const uint32_t slot = h ? hi_base + __popc(bh & lt) : gt + r;
             if (h || (q && r < need)) out[slot] = static_cast<int32_t>(lane + 32 * e);
             hi_base += __popc(bh);
@@ -1847,7 +1859,7 @@ cudaError_t set_smem(K kern, size_t bytes, size_t &configured) {
 template <int DT, int VPT>
 cudaError_t launch_row(const Params &p, cudaStream_t stream) {
     static size_t configured = 0;  // largest dynamic smem opted in so far
-    const size_t bytes = p.plan.row_smem + (p.deterministic ? kDetScratchBytes : 0);
+    const size_t bytes = p.plan.row_smem + (sorted_output(p.deterministic) ? kDetScratchBytes : 0);
     const cudaError_t e = set_smem(row_kernel<DT, VPT>, bytes, configured);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
@@ -1881,7 +1893,7 @@ cudaError_t launch_dt(const Params &p0, cudaStream_t stream) {
         Params p = p0;
         p.row0 = 0;
         p.rows = p0.num_rows;
-        if (!p.deterministic && p.width <= 32 * 64) {  // one warp per row
+        if (!sorted_output(p.deterministic) && p.width <= 32 * 64) {  // one warp per row
             if (p.width <= 32 * 16) return launch_small<DT, 16>(p, stream);
             if (p.width <= 32 * 32) return launch_small<DT, 32>(p, stream);
             return launch_small<DT, 64>(p, stream);

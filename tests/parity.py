@@ -9,7 +9,10 @@ value-multiset comparison"):
   -0.0 and +0.0 identified;
 * returned values are bit copies of logits[idx]; padding holds the lowest
   finite value of the dtype;
-* deterministic mode: the index list is bit-identical to the oracle's.
+* deterministic mode: the index list is bit-identical to the oracle's;
+* a tie mode without the sorted order: the selected index set is the
+  oracle's (the set is unique once the tie mode fixes which of the values
+  equal to the k-th are kept; the order is not).
 """
 from __future__ import annotations
 
@@ -28,7 +31,7 @@ def _norm(v: torch.Tensor) -> torch.Tensor:
 
 def check_rows(logits_cpu: torch.Tensor, n_rows, top_k: int, gpu_idx: torch.Tensor,
                ref_idx: torch.Tensor, gpu_val=None, deterministic: bool = False,
-               rows=None, col0=None) -> None:
+               rows=None, col0=None, same_set: bool = False) -> None:
     """Asserts parity for the given rows (all by default).
 
     ``logits_cpu`` is the [R, W] score matrix, ``n_rows[r]`` the valid count
@@ -49,6 +52,9 @@ def check_rows(logits_cpu: torch.Tensor, n_rows, top_k: int, gpu_idx: torch.Tens
         assert torch.unique(live).numel() == m, f"row {r}: duplicate indices"
         if deterministic:
             assert torch.equal(g, ri[r]), f"row {r}: deterministic index list differs"
+        if same_set:
+            assert torch.equal(torch.sort(live).values, torch.sort(ri[r][:m].long()).values), \
+                f"row {r}: selected index set differs"
         row = logits_cpu[r, c0:c0 + n]
         got = torch.sort(_norm(row[live]), descending=True).values
         ref = torch.sort(_norm(row[ri[r][:m].long()]), descending=True).values

@@ -76,9 +76,30 @@ def _varlen(**kw):
     (dict(ws=None), gb.EWORKSPACE),
     (dict(ws=WS + 16), gb.EWORKSPACE),      # workspace 256-byte aligned
     (dict(ws_bytes=16), gb.EWORKSPACE),
+    (dict(det=gb.TIE_SMALL | gb.TIE_LARGE), gb.EINVAL),   # the tie modes exclude each other
+    (dict(det=gb.SORTED | gb.TIE_SMALL | gb.TIE_LARGE), gb.EINVAL),
+    (dict(det=8), gb.EINVAL),                          # unknown flag
+    (dict(det=-1), gb.EINVAL),
 ])
 def test_varlen_argument_checks(kw, status):
     assert _varlen(**kw) == status
+
+
+@pytest.mark.parametrize("det", [gb.SORTED | gb.TIE_SMALL | gb.TIE_LARGE, 16])
+def test_order_flags_checked_by_every_entry(det):
+    assert _pt(det=det) == gb.EINVAL
+    assert _ragged(det=det) == gb.EINVAL
+    assert _cu(det=det) == gb.EINVAL
+
+
+def test_order_flags_mapping():
+    assert gb.order_flags() == 0
+    assert gb.order_flags(True) == gb.SORTED == 1   # the sorted order alone keeps its meaning
+    assert gb.order_flags(False, "small") == gb.TIE_SMALL
+    assert gb.order_flags(False, "large") == gb.TIE_LARGE
+    assert gb.order_flags(True, "large") == gb.SORTED | gb.TIE_LARGE
+    with pytest.raises(ValueError):
+        gb.order_flags(False, "middle")
 
 
 def test_zero_rows_is_a_noop():

@@ -503,3 +503,98 @@ def test_wider_than_the_plan_is_refused(dev):
     W = 512 * 8192 + 1
     with pytest.raises(gb.GbtopkError):
         gb.gbtopk_plan_query(1, W, 64, torch.float32)
+
+
+# ------------------------------------------------------------------ tie modes
+
+def _tie_rows(W, g):
+    """Rows whose k-th value is shared by many columns: all equal, three
+    values, quarter steps, 1/64 steps of N(0,1), a +-0 mix, and specials."""
+    rows = [torch.full((W,), 1.5),
+            torch.randint(0, 3, (W,), generator=g).float(),
+            torch.round(torch.randn(W, generator=g) * 4) / 4,
+            torch.round(torch.randn(W, generator=g) * 64) / 64]
+    z = torch.zeros(W)
+    z[::2] = -0.0
+    rows.append(z)
+    r = torch.round(torch.randn(W, generator=g) * 8) / 8
+    r[::7] = -0.0
+    r[1::7] = 0.0
+    r[2::97] = float("inf")
+    rows.append(r)
+    return rows
+
+
+def run_tie_case(dev, x, seq, k, tie, sorted_, next_n=1, cr=1):
+    """One top_k_varlen call with a tie mode against the oracle's tie mode:
+    the index list when sorted, else the index set, plus values."""
+    R, W = x.shape
+    n = oracle.row_lengths(seq.tolist(), R, next_n, cr, W)
+    xp = _poisoned(x, n)
+    idx, val = gb.top_k_varlen(xp.to(dev), seq.to(dev), k, next_n=next_n, compress_ratio=cr,
+                               return_values=True, deterministic=sorted_, tie_mode=tie)
+    torch.cuda.synchronize(dev)
+    ref, _ = oracle.topk_varlen_ties(xp, seq, k, tie == "large", next_n=next_n,
+                                     compress_ratio=cr, return_values=False)
+    check_rows(xp, n, k, idx, ref, val, deterministic=sorted_, same_set=True)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("W", [700, 2048, 6000, 50000])
+@pytest.mark.parametrize("tie", ["small", "large"])
+@pytest.mark.parametrize("sorted_", [False, True])
+def test_tie_modes(dev, dtype, W, tie, sorted_):
+    """SMALL / LARGE tie selection with and without the sorted order, on the
+    one-warp rows (W <= 2048 unsorted), the single-block rows and the split
+    pipeline: rows dominated by ties (every boundary size, from a few tied
+    columns to all of them), full and ragged lengths, k from 1 to 2048."""
+    g = torch.Generator().manual_seed(W * 3 + (tie == "large"))
+    rows = _tie_rows(W, g)
+    x = torch.stack(rows + rows).to(dtype)
+    R = x.shape[0]
+    for k in (1, 300, 2048):
+        seq = torch.full((R,), W, dtype=torch.int32)
+        seq[R // 2:] = torch.randint(max(1, min(k // 2, W)), W + 1, (R - R // 2,), generator=g,
+                                     dtype=torch.int32)
+        run_tie_case(dev, x, seq, k, tie, sorted_)
+
+
+@pytest.mark.parametrize("tie,sorted_", [("large", True), ("large", False), ("small", False)])
+def test_tie_modes_dsv32_full(dev, tie, sorted_):
+    """The 64 x 163840 decode batch (logits on a 1/64 grid, so the k-th value
+    is shared) with a tie mode, every row compared."""
+    c = workloads.dsv32_decode()
+    run_tie_case(dev, c.logits, c.seq_lens, c.top_k, tie, sorted_)
+
+
+@pytest.mark.parametrize("tie", ["small", "large"])
+def test_tie_modes_mtp(dev, tie):
+    """next_n = 4, compress_ratio = 4 rows of bf16 logits on a coarse grid."""
+    c = workloads.dsv4_mtp(requests=16, width=20000)
+    x = (torch.round(c.logits.float() * 4) / 4).to(torch.bfloat16)
+    run_tie_case(dev, x, c.seq_lens, c.top_k, tie, False, next_n=c.next_n, cr=c.compress_ratio)
+
+
+@pytest.mark.parametrize("W,k", [(1500, 256), (40000, 2048)])
+def test_ragged_transform_tie_large(dev, W, k):
+    """The ragged-offset epilogue with LARGE ties: back to row-local indices,
+    the set equals the oracle's LARGE selection over each row's window."""
+    R = 24
+    scores, lengths, starts = _ragged_case(R, W, 9100 + W, stride=W + 5)
+    scores = torch.round(scores * 2) / 2                       # heavy ties
+    g = torch.Generator().manual_seed(11)
+    offsets = torch.randint(0, 10_000_000, (R,), generator=g, dtype=torch.int32)
+    out = gb.top_k_ragged_transform(_to_dev_strided(scores, dev), lengths.to(dev),
+                                    offsets.to(dev), k, row_starts=starts.to(dev),
+                                    tie_mode="large")
+    torch.cuda.synchronize(dev)
+    n = [oracle.ragged_length(int(lengths[r]), int(starts[r]), W) for r in range(R)]
+    win = torch.zeros(R, W)
+    for r in range(R):
+        win[r, :n[r]] = scores[r, int(starts[r]):int(starts[r]) + n[r]]
+    ref, _ = oracle.topk_varlen_ties(win, torch.tensor(n, dtype=torch.int32), k, True,
+                                     return_values=False)
+    raw = out.cpu().clone()
+    live = raw >= 0
+    raw[live] -= offsets.view(-1, 1).expand_as(raw)[live]
+    check_rows(win, n, k, raw, ref, None, same_set=True)
