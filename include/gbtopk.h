@@ -40,7 +40,7 @@ extern "C" {
 #define GBTOPK_ETIMEOUT (-7)     /* device flag: a bounded wait gave up (see gbtopk_device_status) */
 
 /* Largest supported top_k. */
-#define GBTOPK_MAX_TOP_K 2048
+#define GBTOPK_MAX_TOP_K 16384
 
 /* Flags of the `deterministic` argument (FlashInfer compact page-table PR
  * body, "SMALL/LARGE tie selection" and the deterministic output order).
@@ -223,12 +223,13 @@ int gbtopk_device_status(void *workspace, uint32_t *flags, void *stream);
 
 /*
  * gbtopk_plan_query — the launch plan for a geometry, for inspection and
- * tests.  Fills out[0..9] = {columns per stream chunk, chunks of the widest
+ * tests.  Fills out[0..10] = {columns per stream chunk, chunks of the widest
  * split row (1 when no row is split), longest row finished by the one-block
  * row kernel, row-kernel shared memory bytes, split (0/1), candidate entries
  * reserved per split row, stream-kernel shared memory bytes, finalize-kernel
- * shared memory bytes, workspace bytes, workspace bytes per row}.  Returns
- * GBTOPK_OK or GBTOPK_EINVAL / GBTOPK_EUNSUPPORTED.
+ * shared memory bytes, workspace bytes, workspace bytes per row, row-kernel
+ * shared memory bytes with GBTOPK_SORTED}.  Returns GBTOPK_OK or
+ * GBTOPK_EINVAL / GBTOPK_EUNSUPPORTED.
  */
 int gbtopk_plan_query(int64_t num_rows, int64_t width, int32_t top_k, int dtype,
                       int64_t *out);

@@ -38,7 +38,7 @@ _lock = threading.Lock()
 
 OK, HINT_DISCARDED = 0, 1
 EINVAL, EALIGN, EOVERLAP, EUNSUPPORTED, ECUDA, EWORKSPACE, ETIMEOUT = -1, -2, -3, -4, -5, -6, -7
-MAX_TOP_K = 2048
+MAX_TOP_K = 16384
 # Flags of the C entry points' `deterministic` argument (include/gbtopk.h).
 SORTED, TIE_SMALL, TIE_LARGE = 1, 2, 4
 
@@ -129,10 +129,10 @@ def gbtopk_workspace_bytes(num_rows: int, width: int, top_k: int, dtype: torch.d
 
 
 def gbtopk_plan_query(num_rows: int, width: int, top_k: int, dtype: torch.dtype) -> dict:
-    out = (ctypes.c_int64 * 10)()
+    out = (ctypes.c_int64 * 11)()
     _check(load_library().gbtopk_plan_query(num_rows, width, top_k, _DTYPES[dtype], out))
     keys = ["chunk", "chunks_per_row", "direct_max", "row_smem", "split", "row_candidates",
-            "stream_smem", "final_smem", "workspace_bytes", "ws_row_bytes"]
+            "stream_smem", "final_smem", "workspace_bytes", "ws_row_bytes", "row_smem_sorted"]
     return dict(zip(keys, list(out)))
 
 

@@ -48,28 +48,36 @@ int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *p
     pl.chunk = static_cast<int32_t>(chunk);
     // histogram (kBins counters) followed by the sample (kSampleSize keys)
     const size_t big_hist = static_cast<size_t>(kBins) * 4 + static_cast<size_t>(kSampleSize) * 4;
-    size_t hist = static_cast<size_t>(sel_cap) * 8;
+    // the selection (sel_cap pairs) aliases the histogram region
+    const size_t sel_bytes = static_cast<size_t>(sel_cap) * 8;
+    const size_t hist = sel_bytes > big_hist ? sel_bytes : big_hist;
     if (width <= 2 * chunk) {
         pl.split = 0;
         pl.direct_max = static_cast<int32_t>(width);
         pl.chunks_per_row = 1;
-        hist = hist > big_hist ? hist : big_hist;
     } else {
         // every row longer than top_k runs through the split pipeline
         pl.split = 1;
         pl.direct_max = top_k;
         pl.chunks_per_row = static_cast<int32_t>((width + chunk - 1) / chunk);
         if (pl.chunks_per_row > kFinalThreads) return GBTOPK_EUNSUPPORTED;
-        hist = hist > big_hist ? hist : big_hist;
         pl.block_rows = num_rows < kMaxBlockRows ? num_rows : kMaxBlockRows;
         // control block, the row table of one launch, the ring (a small
         // batch's stream block still fits beside a row-kernel block)
         pl.stream_smem = kCtrlBytes + align_up(static_cast<size_t>(pl.block_rows + 1) * 16, 128) +
                          static_cast<size_t>(kStages) * kStageBytes;
         // finalize: control, histogram / selection, boundary bin, chunk
-        // offsets, then the gathered candidates (kGatherCandidates)
-        pl.final_smem = kCtrlBytes + kFinalHistBytes + static_cast<size_t>(kFinalBCap) * 8 +
-                        4 * static_cast<size_t>(kFinalThreads) + static_cast<size_t>(kGatherCandidates) * 8;
+        // offsets, then the gathered candidates (up to kGatherCandidates;
+        // the region doubles as the sorted-output scratch)
+        pl.final_sel_bytes = static_cast<size_t>(sel_cap) * 8 > static_cast<size_t>(kFinalHistBytes)
+                                 ? static_cast<size_t>(sel_cap) * 8
+                                 : static_cast<size_t>(kFinalHistBytes);
+        const size_t fixed = kCtrlBytes + pl.final_sel_bytes + static_cast<size_t>(kFinalBCap) * 8 +
+                             4 * static_cast<size_t>(kFinalThreads);
+        size_t gather = static_cast<size_t>(kGatherCandidates) * 8;
+        if (fixed + gather > kMaxSmemBytes) gather = kMaxSmemBytes > fixed ? (kMaxSmemBytes - fixed) / 16 * 16 : 0;
+        if (gather < det_scratch_bytes(sel_cap)) return GBTOPK_EUNSUPPORTED;
+        pl.final_smem = fixed + gather;
         // candidate entries per row: the largest chunks x per-chunk capacity
         // over the row lengths the width allows (capacity shrinks as n grows,
         // so within a chunk count the shortest row is the worst case)
@@ -85,11 +93,18 @@ int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *p
         const size_t seg_off = align_up(kRowInfoBytes + 4 * static_cast<size_t>(pl.chunks_per_row), 16);
         pl.ws_row_bytes = align_up(seg_off + 8 * static_cast<size_t>(entries), 256);
     }
-    // the row kernel stages direct rows only in plans without a split pipeline
+    // the row kernel stages direct rows only in plans without a split
+    // pipeline; the sorted output's scratch reuses the stage (free once the
+    // row is selected)
     const size_t stage = pl.split ? 0 : align_up(static_cast<size_t>(pl.direct_max) * es, 16) + 32;
     pl.off_hist = kCtrlBytes;
     pl.off_stage = align_up(pl.off_hist + hist, 128);
-    pl.row_smem = pl.off_stage + stage;
+    pl.det_bytes = det_scratch_bytes(sel_cap);
+    pl.row_smem_sorted = pl.off_stage + (stage > pl.det_bytes ? stage : pl.det_bytes);
+    // split plans select nothing in the row kernel unless the output is
+    // sorted (short rows are written straight out): histogram and sample only
+    pl.row_smem = pl.split ? align_up(pl.off_hist + big_hist, 128) : pl.off_stage + stage;
+    if (pl.row_smem_sorted > kMaxSmemBytes) return GBTOPK_EUNSUPPORTED;
     pl.ws_bytes = kWsHeaderBytes + static_cast<size_t>(num_rows) * pl.ws_row_bytes;
     *plan = pl;
     return GBTOPK_OK;
@@ -317,6 +332,7 @@ int gbtopk_plan_query(int64_t num_rows, int64_t width, int32_t top_k, int dtype,
     out[7] = static_cast<int64_t>(plan.final_smem);
     out[8] = static_cast<int64_t>(plan.ws_bytes);
     out[9] = static_cast<int64_t>(plan.ws_row_bytes);
+    out[10] = static_cast<int64_t>(plan.row_smem_sorted);
     return GBTOPK_OK;
 }
 

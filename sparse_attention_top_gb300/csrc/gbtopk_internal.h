@@ -27,7 +27,8 @@ constexpr int kFinalHistBytes = 16384; // finalize histogram / selection buffer
 constexpr int kMaxBlockRows = 2048;    // rows per launch of the split pipeline
 constexpr int kFinalBCap = 2048;       // boundary-bin members the finalize kernel can hold
 constexpr int kGatherCandidates = 8192; // candidates the finalize kernel gathers into shared memory
-constexpr size_t kDetScratchBytes = (1u << 12) * 4 + 2048 * 8;  // deterministic output: bin counters + pairs
+constexpr size_t kMaxSmemBytes = 232448;  // dynamic shared memory one block may opt into (227 KB)
+constexpr int kPairSortMax = 2048;     // sorted output copies up to this many pairs, else 16-bit positions
 constexpr size_t kWsHeaderBytes = 256; // device status word + padding
 constexpr size_t kRowInfoBytes = 16;   // t_lo, bin shift (written by the row kernel)
 constexpr uint32_t kSpinLimit = 1u << 22;
@@ -53,6 +54,9 @@ struct Plan {
     int32_t chunks_per_row;  // chunks of the widest split row (0: no split rows possible)
     int32_t split;           // 1 when some row can exceed direct_max
     int32_t sel_cap;         // power of two >= top_k
+    size_t final_sel_bytes;  // finalize histogram / selection region (>= sel_cap pairs)
+    size_t det_bytes;        // sorted-output scratch (det_scratch_bytes(sel_cap))
+    size_t row_smem_sorted;  // row kernel shared memory when the output is sorted
     int32_t stream_grid;     // persistent stream blocks
     int64_t row_seg_entries; // candidate entries reserved per split row
     size_t row_smem, stream_smem, final_smem;
@@ -110,6 +114,13 @@ __host__ __device__ inline int32_t chunk_seg_cap(int64_t n, int32_t k, int32_t c
     const int64_t cap = (3 * static_cast<int64_t>(r) * chunk) / (2 * kSampleSize) + 256;
     const int64_t c = cap < chunk ? cap : chunk;
     return static_cast<int32_t>((c + 63) / 64 * 64);
+}
+
+// Scratch of the sorted output for up to m_cap pairs: kBins counters, then
+// the pairs themselves (m_cap <= kPairSortMax) or 16-bit positions of them.
+__host__ __device__ inline size_t det_scratch_bytes(int32_t m_cap) {
+    const size_t per = m_cap <= kPairSortMax ? 8 : 2;
+    return static_cast<size_t>(kBins) * 4 + ((per * static_cast<size_t>(m_cap) + 15) / 16) * 16;
 }
 
 // Builds the launch plan; returns a gbtopk status.

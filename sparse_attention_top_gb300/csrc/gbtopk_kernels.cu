@@ -33,6 +33,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <type_traits>
 
 #include "gbtopk_internal.h"
 
@@ -567,11 +568,15 @@ __device__ void emit(const Params &p, int64_t row, const uint2 *sel, int m) {
 // each bin's first slot, the pairs are scattered into their bins' segments
 // (scratch), and each pair's slot is its segment's start plus the number of
 // segment mates that order before it.  Slots m .. k-1 get -1.  `scratch`
-// holds kBins counters and m pairs (kDetScratchBytes).  All threads call it.
-template <int DT>
-__device__ void emit_sorted(const Params &p, int64_t row, const uint2 *sel, int m, uint8_t *scratch, Ctrl &c) {
+// holds kBins counters, then the segments: copies of the pairs, or (Compact,
+// for m up to 2^16) their 16-bit positions in sel, det_scratch_bytes(m)
+// bytes in all.  All threads call it.
+template <int DT, bool Compact>
+__device__ void emit_sorted_impl(const Params &p, int64_t row, const uint2 *sel, int m, uint8_t *scratch,
+                                 Ctrl &c) {
+    using seg_t = typename std::conditional<Compact, uint16_t, uint2>::type;
     uint32_t *bins = reinterpret_cast<uint32_t *>(scratch);
-    uint2 *seg = reinterpret_cast<uint2 *>(scratch + kBins * 4);
+    seg_t *seg = reinterpret_cast<seg_t *>(scratch + kBins * 4);
     const int nt = blockDim.x;
     const int tid = threadIdx.x;
     const RowEpi ep = row_epilogue(p, row);
@@ -611,19 +616,25 @@ __device__ void emit_sorted(const Params &p, int64_t row, const uint2 *sel, int 
     __syncthreads();
     for (int i = tid; i < m; i += nt) {
         const uint2 v = sel[i];
-        seg[atomicAdd(&bins[(Elem<DT>::key(v.x) - kmin) >> shift], 1u)] = v;
+        const uint32_t at = atomicAdd(&bins[(Elem<DT>::key(v.x) - kmin) >> shift], 1u);
+        if constexpr (Compact) seg[at] = static_cast<uint16_t>(i);
+        else seg[at] = v;
     }
     __syncthreads();
+    auto pair_at = [&](uint32_t j) -> uint2 {
+        if constexpr (Compact) return sel[seg[j]];
+        else return seg[j];
+    };
     // bins[b] now ends b's segment, which starts where b + 1's ends
     for (int j = tid; j < m; j += nt) {
-        const uint2 v = seg[j];
+        const uint2 v = pair_at(j);
         const int b = static_cast<int>((Elem<DT>::key(v.x) - kmin) >> shift);
         const uint32_t lo = b == kBins - 1 ? 0u : bins[b + 1], hi = bins[b];
         const unsigned long long mine = (static_cast<unsigned long long>(Elem<DT>::key(v.x)) << 32) |
                                         static_cast<unsigned long long>(0xFFFFFFFFu - v.y);
         uint32_t before = 0;
         for (uint32_t i = lo; i < hi; ++i) {
-            const uint2 o = seg[i];
+            const uint2 o = pair_at(i);
             const unsigned long long oc = (static_cast<unsigned long long>(Elem<DT>::key(o.x)) << 32) |
                                           static_cast<unsigned long long>(0xFFFFFFFFu - o.y);
             before += oc > mine ? 1u : 0u;
@@ -632,6 +643,13 @@ __device__ void emit_sorted(const Params &p, int64_t row, const uint2 *sel, int 
     }
     for (int j = m + tid; j < p.k; j += nt) put_slot<DT>(p, row, ep, j, -1, 0u);
     __syncthreads();
+}
+
+// The sorted output with the segment form the plan's scratch was sized for.
+template <int DT>
+__device__ void emit_sorted(const Params &p, int64_t row, const uint2 *sel, int m, uint8_t *scratch, Ctrl &c) {
+    if (p.plan.sel_cap <= kPairSortMax) emit_sorted_impl<DT, false>(p, row, sel, m, scratch, c);
+    else emit_sorted_impl<DT, true>(p, row, sel, m, scratch, c);
 }
 
 // ---------------------------------------------------------------- bulk staging
@@ -990,8 +1008,7 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
     uint32_t *hist = reinterpret_cast<uint32_t *>(smem + p.plan.off_hist);
     uint2 *sel = reinterpret_cast<uint2 *>(smem + p.plan.off_hist);  // aliases hist
     uint32_t *sample = reinterpret_cast<uint32_t *>(smem + p.plan.off_hist + kBins * 4);
-    uint8_t *stage = smem + p.plan.off_stage;
-    const uint32_t stage_pairs = static_cast<uint32_t>((p.plan.row_smem - p.plan.off_stage) / sizeof(uint2));
+    uint8_t *stage = smem + p.plan.off_stage;  // direct rows; the sorted output's scratch
     const int64_t row = p.row0 + blockIdx.x;
     const int k = p.k;
     const bool sorted = sorted_output(p.deterministic);
@@ -1092,12 +1109,18 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
 
     // ---- short and empty rows: every valid column, then -1
     if (n <= k) {
-        const bool need_raw = sorted || p.out_val != nullptr;
-        for (int j = threadIdx.x; j < n; j += blockDim.x)
-            sel[j] = make_uint2(need_raw ? ldg_raw(xrow + j) : 0u, static_cast<uint32_t>(j));
-        __syncthreads();
-        if (sorted) emit_sorted<DT>(p, row, sel, static_cast<int>(n), smem + p.plan.row_smem, c);
-        else emit<DT>(p, row, sel, static_cast<int>(n));
+        if (sorted) {
+            for (int j = threadIdx.x; j < n; j += blockDim.x)
+                sel[j] = make_uint2(ldg_raw(xrow + j), static_cast<uint32_t>(j));
+            __syncthreads();
+            emit_sorted<DT>(p, row, sel, static_cast<int>(n), stage, c);
+        } else {
+            const RowEpi ep = row_epilogue(p, row);
+            for (int j = threadIdx.x; j < k; j += blockDim.x) {
+                const bool live = j < n;
+                put_slot<DT>(p, row, ep, j, live ? j : -1, live && p.out_val ? ldg_raw(xrow + j) : 0u);
+            }
+        }
         GBTOPK_TRACE_POINT(6, 0);
         GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | 1u);
         return;
@@ -1107,6 +1130,7 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
     if constexpr (VPT == 0) {
         return;  // split plans: every row longer than top_k went to the guess above
     } else {
+    const uint32_t stage_pairs = static_cast<uint32_t>((p.plan.row_smem - p.plan.off_stage) / sizeof(uint2));
     if (threadIdx.x == 0) mbar_init(&c.bar);
     __syncthreads();
     const Span sp = span_of<DT>(xrow, n);
@@ -1146,9 +1170,13 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
                                                         k, tie, sel, lcand + total, stage_pairs - total, c);
     }
     if (!done) exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, tie, sel, c.rhist, c);
-    if (sorted) emit_sorted<DT>(p, row, sel, k, smem + p.plan.row_smem, c);
-    else emit<DT>(p, row, sel, k);
-    if (!ok && threadIdx.x == 0) mbar_wait(&c.bar, 0);  // let the copy land before exit
+    if (!ok && threadIdx.x == 0) mbar_wait(&c.bar, 0);  // let the copy land before reusing the stage
+    if (sorted) {
+        __syncthreads();
+        emit_sorted<DT>(p, row, sel, k, stage, c);  // the stage is free once the row is selected
+    } else {
+        emit<DT>(p, row, sel, k);
+    }
     GBTOPK_TRACE_POINT(6, 0);
     GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | 2u);
     }
@@ -1611,16 +1639,15 @@ __device__ bool select_from_segments(const SegMap &map, uint32_t total, uint32_t
 template <int DT>
 __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_constant__ Params p) {
     using raw_t = typename Elem<DT>::raw_t;
-    constexpr int GB = 8;  // candidates in flight per thread (L2 path)
     extern __shared__ __align__(128) uint8_t smem[];
     Ctrl &c = *reinterpret_cast<Ctrl *>(smem);
     uint32_t *hist = reinterpret_cast<uint32_t *>(smem + kCtrlBytes);
     uint2 *sel = reinterpret_cast<uint2 *>(smem + kCtrlBytes);  // aliases hist
-    uint2 *blist = reinterpret_cast<uint2 *>(smem + kCtrlBytes + kFinalHistBytes);
+    uint2 *blist = reinterpret_cast<uint2 *>(smem + kCtrlBytes + p.plan.final_sel_bytes);
     uint32_t *choff = reinterpret_cast<uint32_t *>(blist + kFinalBCap);
     uint2 *cand = reinterpret_cast<uint2 *>(choff + kFinalThreads);  // gathered candidates
     const uint32_t gather_cap = static_cast<uint32_t>(
-        (p.plan.final_smem - (kCtrlBytes + kFinalHistBytes + static_cast<size_t>(kFinalBCap) * 8 +
+        (p.plan.final_smem - (kCtrlBytes + p.plan.final_sel_bytes + static_cast<size_t>(kFinalBCap) * 8 +
                               4 * static_cast<size_t>(kFinalThreads))) / sizeof(uint2));
     const int64_t row = p.row0 + blockIdx.x;
     const int k = p.k;
@@ -1859,7 +1886,7 @@ cudaError_t set_smem(K kern, size_t bytes, size_t &configured) {
 template <int DT, int VPT>
 cudaError_t launch_row(const Params &p, cudaStream_t stream) {
     static size_t configured = 0;  // largest dynamic smem opted in so far
-    const size_t bytes = p.plan.row_smem + (sorted_output(p.deterministic) ? kDetScratchBytes : 0);
+    const size_t bytes = sorted_output(p.deterministic) ? p.plan.row_smem_sorted : p.plan.row_smem;
     const cudaError_t e = set_smem(row_kernel<DT, VPT>, bytes, configured);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];

@@ -129,7 +129,7 @@ def _pt(**kw):
     (dict(pt_row_stride=8), gb.EINVAL),
     (dict(out_raw=A + 16384 + 32), gb.EOVERLAP),
     (dict(out_raw=A + 32772), gb.EALIGN),
-    (dict(top_k=4096), gb.EUNSUPPORTED),
+    (dict(top_k=gb.MAX_TOP_K + 1), gb.EUNSUPPORTED),
     (dict(ws_bytes=0), gb.EWORKSPACE),
 ])
 def test_page_table_argument_checks(kw, status):
@@ -144,13 +144,15 @@ def test_plan_totality_and_consistency():
     for trial in range(3000):
         R = rnd.choice([1, 2, 4, 16, 64, 256, 1024, 4096, rnd.randint(1, 5000)])
         W = rnd.choice(widths + [rnd.randint(1, 1 << 19)])
-        k = rnd.choice([1, 2, 64, 512, 1024, 2048, rnd.randint(1, 2048)])
+        k = rnd.choice([1, 2, 64, 512, 1024, 2048, rnd.randint(1, 2048), 2049, 4096, 16384,
+                        rnd.randint(1, gb.MAX_TOP_K)])
         dt = rnd.choice(dts)
         p = gb.gbtopk_plan_query(R, W, k, dt)
         es = 4 if dt == torch.float32 else 2
         assert p["chunk"] * es == 32768
-        for key in ("row_smem", "stream_smem", "final_smem"):
+        for key in ("row_smem", "row_smem_sorted", "stream_smem", "final_smem"):
             assert p[key] <= 227 * 1024
+        assert p["row_smem_sorted"] >= p["row_smem"]
         # on small batches a stream block and a row block fit on one SM together
         if p["split"] and R <= 128:
             assert p["row_smem"] + p["stream_smem"] + 2048 <= 228 * 1024
@@ -189,7 +191,7 @@ def _ragged(**kw):
     (dict(offsets=None), gb.EINVAL),
     (dict(lengths=None), gb.EINVAL),
     (dict(out=A + 16388), gb.EALIGN),
-    (dict(top_k=4096), gb.EUNSUPPORTED),
+    (dict(top_k=gb.MAX_TOP_K + 1), gb.EUNSUPPORTED),
     (dict(ws_bytes=0), gb.EWORKSPACE),
 ])
 def test_ragged_argument_checks(kw, status):

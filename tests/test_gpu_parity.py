@@ -598,3 +598,53 @@ def test_ragged_transform_tie_large(dev, W, k):
     live = raw >= 0
     raw[live] -= offsets.view(-1, 1).expand_as(raw)[live]
     check_rows(win, n, k, raw, ref, None, same_set=True)
+
+
+# ------------------------------------------------------------------ top_k beyond 2048
+
+def _large_k_rows(R, W, g):
+    x = torch.randn(R, W, generator=g)
+    x[1] = torch.round(x[1] * 64) / 64                     # 1/64 grid, as the decode batch
+    x[1, torch.randperm(W, generator=g)[:W // 100]] += 4.0
+    x[2] = torch.round(x[2] * 4) / 4                       # heavy ties
+    x[3, ::5] = float("inf")
+    x[3, 1::5] = -0.0
+    x[3, 2::5] = 0.0
+    x[4] = 0.75                                            # all equal
+    return x
+
+
+@pytest.mark.parametrize("W,k,dtype", [(163840, 4096, torch.float32), (163840, 16384, torch.float32),
+                                       (65536, 8192, torch.bfloat16), (30000, 16384, torch.float16),
+                                       (16384, 4096, torch.float32), (16384, 12000, torch.float32),
+                                       (1500, 4000, torch.float32)])
+@pytest.mark.parametrize("sorted_", [False, True])
+def test_large_top_k(dev, W, k, dtype, sorted_):
+    """top_k from 4096 to 16384 (FlashInfer radix_filter's range): split rows
+    whose candidates overflow the shared gather (finalize from the segments
+    in L2), one-block rows with selections of up to 12000 pairs, short rows;
+    ties, specials and an all-equal row; every row compared."""
+    g = torch.Generator().manual_seed(W + k)
+    R = 10
+    x = _large_k_rows(R, W, g)
+    lens = torch.randint(1, W + 1, (R,), generator=g, dtype=torch.int32)
+    lens[:5] = W
+    lens[5], lens[6], lens[7] = min(k - 1, W), min(k, W), min(k + 1, W)
+    c = workloads.VarlenCase("large_k", x.to(dtype), lens, k)
+    run_case(dev, c, det=sorted_, values=True)
+
+
+@pytest.mark.parametrize("tie,sorted_", [("large", False), ("large", True), ("small", False)])
+def test_large_top_k_tie_modes(dev, tie, sorted_):
+    g = torch.Generator().manual_seed(77)
+    W, k = 163840, 16384
+    x = torch.round(torch.randn(6, W, generator=g) * 16) / 16
+    seq = torch.tensor([W, W, 20000, 16385, 16384, 90000], dtype=torch.int32)
+    run_tie_case(dev, x, seq, k, tie, sorted_)
+
+
+def test_large_top_k_page_table(dev):
+    """The compact page-table transform (sorted, out and out_raw) at top_k 8192."""
+    c = workloads.page_table_case(rows=32, width=32768, row_stride=33024, page_size=64,
+                                  pt_cols=1024, top_k=8192, seed=5099)
+    _run_page_table(dev, c)
