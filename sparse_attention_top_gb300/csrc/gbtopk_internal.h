@@ -117,9 +117,10 @@ __host__ __device__ inline int32_t chunk_seg_cap(int64_t n, int32_t k, int32_t c
 }
 
 // Scratch of the sorted output for up to m_cap pairs: kBins counters, then
-// the pairs themselves (m_cap <= kPairSortMax) or 16-bit positions of them.
+// a 64-bit order key, a 16-bit position and a 16-bit inverse-map entry per
+// pair (m_cap <= kPairSortMax), or the positions alone.
 __host__ __device__ inline size_t det_scratch_bytes(int32_t m_cap) {
-    const size_t per = m_cap <= kPairSortMax ? 8 : 2;
+    const size_t per = m_cap <= kPairSortMax ? 12 : 2;
     return static_cast<size_t>(kBins) * 4 + ((per * static_cast<size_t>(m_cap) + 15) / 16) * 16;
 }
 

@@ -33,7 +33,6 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
-#include <type_traits>
 
 #include "gbtopk_internal.h"
 
@@ -208,6 +207,45 @@ __device__ __forceinline__ void block_minmax(uint32_t kmin, uint32_t kmax, Ctrl 
     if (lane_id() == 0) {
         atomicMin(&c.key_min, kmin);
         atomicMax(&c.key_max, kmax);
+    }
+    __syncthreads();
+}
+
+// Counts from the top over NB counters: calls f(b, above, cnt) once for every
+// bin b, with above = the sum of the counts of the bins > b.  Thread t owns
+// the run of NB / NT bins that follows thread t - 1's from the top and reads
+// it with vector loads (at most 2-way bank conflicts); one block scan of the
+// runs' sums gives each run its start.  Ends with a barrier (the counters
+// may be rewritten by f; c.scan is free again).
+template <int NT, int NB, class F>
+__device__ __forceinline__ void scan_from_top(const uint32_t *hist, Ctrl &c, F f) {
+    constexpr int BPT = NB / NT;
+    static_assert(BPT * NT == NB && (BPT == 2 || BPT % 4 == 0), "bins per thread");
+    const int lo = NB - BPT * (static_cast<int>(threadIdx.x) + 1);  // lowest bin of the run
+    uint32_t cnt[BPT];
+    if constexpr (BPT == 2) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(hist + lo);
+        cnt[0] = v.x;
+        cnt[1] = v.y;
+    } else {
+#pragma unroll
+        for (int q = 0; q < BPT / 4; ++q) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(hist + lo + 4 * q);
+            cnt[4 * q] = v.x;
+            cnt[4 * q + 1] = v.y;
+            cnt[4 * q + 2] = v.z;
+            cnt[4 * q + 3] = v.w;
+        }
+    }
+    uint32_t sum = 0;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) sum += cnt[j];
+    uint32_t tot;
+    uint32_t above = block_excl_scan(sum, c, tot);
+#pragma unroll
+    for (int j = BPT - 1; j >= 0; --j) {
+        f(static_cast<uint32_t>(lo + j), above, cnt[j]);
+        above += cnt[j];
     }
     __syncthreads();
 }
@@ -543,14 +581,19 @@ __device__ __forceinline__ int32_t out_index(const Params &p, const RowEpi &e, i
 // (when given), and the value (bit copy, or the dtype's lowest finite value
 // for a -1 slot).
 template <int DT>
-__device__ __forceinline__ void put_slot(const Params &p, int64_t row, const RowEpi &e, int j, int32_t idx,
-                                         uint32_t raw) {
+__device__ __forceinline__ void put_mapped(const Params &p, int64_t row, int j, int32_t oi, int32_t idx,
+                                           uint32_t raw) {
     using raw_t = typename Elem<DT>::raw_t;
     const int k = p.k;
-    p.out_idx[row * k + j] = out_index(p, e, idx);
+    p.out_idx[row * k + j] = oi;
     if (p.out_raw) p.out_raw[row * k + j] = idx;
     if (p.out_val)
         static_cast<raw_t *>(p.out_val)[row * k + j] = static_cast<raw_t>(idx >= 0 ? raw : Elem<DT>::kLowest);
+}
+template <int DT>
+__device__ __forceinline__ void put_slot(const Params &p, int64_t row, const RowEpi &e, int j, int32_t idx,
+                                         uint32_t raw) {
+    put_mapped<DT>(p, row, j, out_index(p, e, idx), idx, raw);
 }
 
 template <int DT>
@@ -562,94 +605,106 @@ __device__ void emit(const Params &p, int64_t row, const uint2 *sel, int m) {
     }
 }
 
+// Order key of a selected (raw, column) pair in the deterministic output:
+// (key << 32) | ~column, larger first (value desc, then column asc).
+template <int DT>
+__device__ __forceinline__ unsigned long long sort_composite(uint2 v) {
+    return (static_cast<unsigned long long>(Elem<DT>::key(v.x)) << 32) |
+           static_cast<unsigned long long>(0xFFFFFFFFu - v.y);
+}
+
 // Deterministic output (value desc, column asc) of the m selected pairs in
 // sel, written straight to their output slots.  The keys are counted in
-// kBins bins over their own range; an exclusive scan from the top gives
-// each bin's first slot, the pairs are scattered into their bins' segments
-// (scratch), and each pair's slot is its segment's start plus the number of
-// segment mates that order before it.  Slots m .. k-1 get -1.  `scratch`
-// holds kBins counters, then the segments: copies of the pairs, or (Compact,
-// for m up to 2^16) their 16-bit positions in sel, det_scratch_bytes(m)
-// bytes in all.  All threads call it.
-template <int DT, bool Compact>
+// kBins bins over their own range; a scan from the top gives each bin's
+// first slot; the pairs are scattered into their bins' segments (scratch)
+// and each pair's slot is its segment's start plus the number of segment
+// mates with a larger sort_composite.  Slots m .. k-1 get -1.  `scratch`
+// holds kBins counters, then the segments: the composites, the 16-bit
+// positions of their pairs in sel and the inverse map (slot -> position),
+// or (Compact) the positions alone, the composites being recomputed
+// (det_scratch_bytes(sel_cap) bytes in all).  All NT threads call it.
+template <int DT, int NT, bool Compact>
 __device__ void emit_sorted_impl(const Params &p, int64_t row, const uint2 *sel, int m, uint8_t *scratch,
                                  Ctrl &c) {
-    using seg_t = typename std::conditional<Compact, uint16_t, uint2>::type;
     uint32_t *bins = reinterpret_cast<uint32_t *>(scratch);
-    seg_t *seg = reinterpret_cast<seg_t *>(scratch + kBins * 4);
-    const int nt = blockDim.x;
+    unsigned long long *comp = reinterpret_cast<unsigned long long *>(scratch + kBins * 4);
+    uint16_t *pos = reinterpret_cast<uint16_t *>(
+        scratch + kBins * 4 + (Compact ? 0 : 8 * static_cast<size_t>(p.plan.sel_cap)));
     const int tid = threadIdx.x;
     const RowEpi ep = row_epilogue(p, row);
     if (tid == 0) {
         c.key_min = 0xFFFFFFFFu;
         c.key_max = 0;
     }
-    for (int b = tid; b < kBins; b += nt) bins[b] = 0;
+    for (int b = tid; b < kBins; b += NT) bins[b] = 0;
     __syncthreads();
     uint32_t kmin = 0xFFFFFFFFu, kmax = 0;
-    for (int i = tid; i < m; i += nt) {
+    for (int i = tid; i < m; i += NT) {
         const uint32_t key = Elem<DT>::key(sel[i].x);
         kmin = key < kmin ? key : kmin;
         kmax = key > kmax ? key : kmax;
     }
     block_minmax(kmin, kmax, c);
+    if (NT == kFinalThreads && tid == 0) GBTOPK_TRACE_SET(40960 + blockIdx.x, 3, -1);
     kmin = c.key_min;
     const int bits = 32 - __clz(c.key_max - kmin);
     const int shift = bits > kBinBits ? bits - kBinBits : 0;
-    for (int i = tid; i < m; i += nt)
+    for (int i = tid; i < m; i += NT)
         atomicAdd(&bins[(Elem<DT>::key(sel[i].x) - kmin) >> shift], 1u);
     __syncthreads();
-    // exclusive scan from the top: bins[b] = pairs in the bins above b
-    {
-        const int bpt = kBins / nt;  // bins per thread, from the top down
-        uint32_t sum = 0;
-        for (int j = 0; j < bpt; ++j) sum += bins[kBins - 1 - bpt * tid - j];
-        uint32_t tot;
-        uint32_t run = block_excl_scan(sum, c, tot);
-        for (int j = 0; j < bpt; ++j) {
-            const int b = kBins - 1 - bpt * tid - j;
-            const uint32_t cnt = bins[b];
-            bins[b] = run;
-            run += cnt;
-        }
-    }
-    __syncthreads();
-    for (int i = tid; i < m; i += nt) {
+    // bins[b] = pairs in the bins above b
+    scan_from_top<NT, kBins>(bins, c, [&](uint32_t b, uint32_t above, uint32_t) { bins[b] = above; });
+    if (NT == kFinalThreads && tid == 0) GBTOPK_TRACE_SET(40960 + blockIdx.x, 4, -1);
+    for (int i = tid; i < m; i += NT) {
         const uint2 v = sel[i];
         const uint32_t at = atomicAdd(&bins[(Elem<DT>::key(v.x) - kmin) >> shift], 1u);
-        if constexpr (Compact) seg[at] = static_cast<uint16_t>(i);
-        else seg[at] = v;
+        pos[at] = static_cast<uint16_t>(i);
+        if constexpr (!Compact) comp[at] = sort_composite<DT>(v);
     }
     __syncthreads();
-    auto pair_at = [&](uint32_t j) -> uint2 {
-        if constexpr (Compact) return sel[seg[j]];
-        else return seg[j];
-    };
+    if (NT == kFinalThreads && tid == 0) GBTOPK_TRACE_SET(40960 + blockIdx.x, 5, -1);
     // bins[b] now ends b's segment, which starts where b + 1's ends
-    for (int j = tid; j < m; j += nt) {
-        const uint2 v = pair_at(j);
-        const int b = static_cast<int>((Elem<DT>::key(v.x) - kmin) >> shift);
-        const uint32_t lo = b == kBins - 1 ? 0u : bins[b + 1], hi = bins[b];
-        const unsigned long long mine = (static_cast<unsigned long long>(Elem<DT>::key(v.x)) << 32) |
-                                        static_cast<unsigned long long>(0xFFFFFFFFu - v.y);
-        uint32_t before = 0;
-        for (uint32_t i = lo; i < hi; ++i) {
-            const uint2 o = pair_at(i);
-            const unsigned long long oc = (static_cast<unsigned long long>(Elem<DT>::key(o.x)) << 32) |
-                                          static_cast<unsigned long long>(0xFFFFFFFFu - o.y);
-            before += oc > mine ? 1u : 0u;
+    if constexpr (Compact) {
+        // rank and write in one pass (no room for an inverse map)
+        for (int j = tid; j < m; j += NT) {
+            const uint2 v = sel[pos[j]];
+            const int32_t oi = out_index(p, ep, static_cast<int32_t>(v.y));  // overlaps the ranking
+            const unsigned long long mine = sort_composite<DT>(v);
+            const int b = static_cast<int>((static_cast<uint32_t>(mine >> 32) - kmin) >> shift);
+            const uint32_t lo = b == kBins - 1 ? 0u : bins[b + 1], hi = bins[b];
+            uint32_t before = 0;
+            for (uint32_t i = lo; i < hi; ++i) before += sort_composite<DT>(sel[pos[i]]) > mine ? 1u : 0u;
+            put_mapped<DT>(p, row, static_cast<int>(lo + before), oi, static_cast<int32_t>(v.y), v.x);
         }
-        put_slot<DT>(p, row, ep, static_cast<int>(lo + before), static_cast<int32_t>(v.y), v.x);
+    } else {
+        // rank into an inverse map (slot -> position in sel), then write the
+        // slots in order: coalesced stores, independent page-table loads
+        uint16_t *inv = pos + p.plan.sel_cap;
+        for (int j = tid; j < m; j += NT) {
+            const unsigned long long mine = comp[j];
+            const int b = static_cast<int>((static_cast<uint32_t>(mine >> 32) - kmin) >> shift);
+            const uint32_t lo = b == kBins - 1 ? 0u : bins[b + 1], hi = bins[b];
+            uint32_t before = 0;
+            for (uint32_t i = lo; i < hi; ++i) before += comp[i] > mine ? 1u : 0u;
+            inv[lo + before] = pos[j];
+        }
+        __syncthreads();
+        if (NT == kFinalThreads && tid == 0) GBTOPK_TRACE_SET(40960 + blockIdx.x, 8, -1);
+#pragma unroll 4
+        for (int j = tid; j < m; j += NT) {
+            const uint2 v = sel[inv[j]];
+            put_slot<DT>(p, row, ep, j, static_cast<int32_t>(v.y), v.x);
+        }
     }
-    for (int j = m + tid; j < p.k; j += nt) put_slot<DT>(p, row, ep, j, -1, 0u);
+    for (int j = m + tid; j < p.k; j += NT) put_mapped<DT>(p, row, j, -1, -1, 0u);
     __syncthreads();
 }
 
 // The sorted output with the segment form the plan's scratch was sized for.
-template <int DT>
+template <int DT, int NT>
 __device__ void emit_sorted(const Params &p, int64_t row, const uint2 *sel, int m, uint8_t *scratch, Ctrl &c) {
-    if (p.plan.sel_cap <= kPairSortMax) emit_sorted_impl<DT, false>(p, row, sel, m, scratch, c);
-    else emit_sorted_impl<DT, true>(p, row, sel, m, scratch, c);
+    if (p.plan.sel_cap <= kPairSortMax) emit_sorted_impl<DT, NT, false>(p, row, sel, m, scratch, c);
+    else emit_sorted_impl<DT, NT, true>(p, row, sel, m, scratch, c);
 }
 
 // ---------------------------------------------------------------- bulk staging
@@ -785,29 +840,13 @@ __device__ __forceinline__ uint32_t valid_lanes(int v, int nvec, int off, int le
 // c.bcast[4].  Requires 1 <= r <= sum of counts.
 template <int NT, int NB = kBins>
 __device__ void find_bin_from_top(const uint32_t *hist, uint32_t r, Ctrl &c) {
-    constexpr int BPT = NB / NT;
-    uint32_t local[BPT], s = 0;
-#pragma unroll
-    for (int j = 0; j < BPT; ++j) {
-        local[j] = hist[NB - 1 - BPT * threadIdx.x - j];
-        s += local[j];
-    }
-    uint32_t tot;
-    const uint32_t excl = block_excl_scan(s, c, tot);
-    if (excl < r && r <= excl + s) {
-        uint32_t acc = excl;
-#pragma unroll
-        for (int j = 0; j < BPT; ++j) {
-            if (acc + local[j] >= r) {
-                c.bcast[2] = NB - 1 - BPT * threadIdx.x - j;
-                c.bcast[3] = acc;
-                c.bcast[4] = local[j];
-                break;
-            }
-            acc += local[j];
+    scan_from_top<NT, NB>(hist, c, [&](uint32_t b, uint32_t above, uint32_t cnt) {
+        if (above < r && r <= above + cnt) {
+            c.bcast[2] = b;
+            c.bcast[3] = above;
+            c.bcast[4] = cnt;
         }
-    }
-    __syncthreads();
+    });
 }
 
 // Conservative rank-r threshold of m keys in shared memory whose range is
@@ -1113,7 +1152,7 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
             for (int j = threadIdx.x; j < n; j += blockDim.x)
                 sel[j] = make_uint2(ldg_raw(xrow + j), static_cast<uint32_t>(j));
             __syncthreads();
-            emit_sorted<DT>(p, row, sel, static_cast<int>(n), stage, c);
+            emit_sorted<DT, kThreads>(p, row, sel, static_cast<int>(n), stage, c);
         } else {
             const RowEpi ep = row_epilogue(p, row);
             for (int j = threadIdx.x; j < k; j += blockDim.x) {
@@ -1173,7 +1212,7 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
     if (!ok && threadIdx.x == 0) mbar_wait(&c.bar, 0);  // let the copy land before reusing the stage
     if (sorted) {
         __syncthreads();
-        emit_sorted<DT>(p, row, sel, k, stage, c);  // the stage is free once the row is selected
+        emit_sorted<DT, kThreads>(p, row, sel, k, stage, c);  // the stage is free once the row is selected
     } else {
         emit<DT>(p, row, sel, k);
     }
@@ -1519,16 +1558,14 @@ __device__ bool rank_boundary(const uint2 *blist, uint32_t bsize, uint32_t need,
 // histogrammed over kBins bins (bin_of), the bin b* holding the k-th key
 // from the top is found, the candidates of higher bins go to sel and b*'s
 // members to blist, ranked by (key desc, column asc) so the best `need`
-// complete sel[0, k).  `sel` may alias `hist`.  All NT threads of the block
-// call it; returns false (nothing written) when b* holds more than
-// kFinalBCap members.
+// complete sel[0, k).  `sel` may alias `hist`, whose kBins counters the
+// caller has zeroed.  All NT threads of the block call it; returns false
+// (nothing written) when b* holds more than kFinalBCap members.
 template <int DT, int NT>
 __device__ bool select_gathered(const uint2 *cand, uint32_t total_p, uint32_t t_lo, int bin_shift, int k,
                                 int tie, uint32_t *hist, uint2 *sel, uint2 *blist, Ctrl &c) {
     const uint32_t tid = threadIdx.x;
-#pragma unroll
-    for (int j = 0; j < kBins / NT; ++j) hist[tid + j * NT] = 0;
-    __syncthreads();
+#pragma unroll 4
     for (uint32_t i = tid; i < total_p; i += NT) {
         const uint2 v = cand[i];
         if (v.y != kPadColumn) atomicAdd(&hist[bin_of(Elem<DT>::key(v.x), t_lo, bin_shift)], 1u);
@@ -1538,13 +1575,10 @@ __device__ bool select_gathered(const uint2 *cand, uint32_t total_p, uint32_t t_
     const uint32_t bstar = c.bcast[2], above = c.bcast[3], bsize = c.bcast[4];
     if (bsize > static_cast<uint32_t>(kFinalBCap)) return false;
     // bins above b* go to sel, bin b* to blist (sel aliases the consumed
-    // histogram): each thread counts its candidates (a contiguous run), one
-    // block scan gives its output slots
-    const uint32_t per = (total_p + NT - 1) / NT;
-    const uint32_t i_lo = tid * per < total_p ? tid * per : total_p;
-    const uint32_t i_hi = i_lo + per < total_p ? i_lo + per : total_p;
+    // histogram): each thread counts its candidates (every NT-th, so a
+    // warp's loads are consecutive), one block scan gives its output slots
     uint32_t nhi = 0, neq = 0;
-    for (uint32_t i = i_lo; i < i_hi; ++i) {
+    for (uint32_t i = tid; i < total_p; i += NT) {
         const uint2 v = cand[i];
         const uint32_t b = bin_of(Elem<DT>::key(v.x), t_lo, bin_shift);
         const bool live = v.y != kPadColumn;
@@ -1554,7 +1588,7 @@ __device__ bool select_gathered(const uint2 *cand, uint32_t total_p, uint32_t t_
     uint32_t ptot;
     const uint32_t pre = block_excl_scan((nhi << 16) | neq, c, ptot);
     uint32_t hs = pre >> 16, es = pre & 0xFFFFu;
-    for (uint32_t i = i_lo; i < i_hi && (nhi | neq); ++i) {
+    for (uint32_t i = tid; i < total_p && (nhi | neq); i += NT) {
         const uint2 v = cand[i];
         if (v.y == kPadColumn) continue;
         const uint32_t b = bin_of(Elem<DT>::key(v.x), t_lo, bin_shift);
@@ -1701,6 +1735,9 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
                 "l"(segs + static_cast<int64_t>(tid) * cap), "r"(padded * 8u), "r"(smem_u32(&c.bar))
                 : "memory");
         }
+        // zero the histogram while the copies land (it is not their destination)
+#pragma unroll
+        for (int j = 0; j < kBins / kFinalThreads; ++j) hist[tid + j * kFinalThreads] = 0;
         copy_ok = wait_bar(p.ws, c, &c.bar, 0);
         if (copy_ok) {
             if (tid < nch && (cnt & 1u)) cand[poff + cnt].y = kPadColumn;
@@ -1728,7 +1765,7 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
     if (!copy_ok && tid == 0) mbar_wait(&c.bar, 0);  // let the copies land (before reusing cand)
     if (sorted) {
         __syncthreads();
-        emit_sorted<DT>(p, row, sel, k, reinterpret_cast<uint8_t *>(cand), c);
+        emit_sorted<DT, kFinalThreads>(p, row, sel, k, reinterpret_cast<uint8_t *>(cand), c);
     } else {
         emit<DT>(p, row, sel, k);
     }
