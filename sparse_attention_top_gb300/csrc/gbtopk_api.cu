@@ -46,11 +46,13 @@ int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *p
     while (sel_cap < top_k) sel_cap <<= 1;
     pl.sel_cap = sel_cap;
     pl.chunk = static_cast<int32_t>(chunk);
-    // histogram (kBins counters) followed by the sample (kSampleSize keys)
-    const size_t big_hist = static_cast<size_t>(kBins) * 4 + static_cast<size_t>(kSampleSize) * 4;
-    // the selection (sel_cap pairs) aliases the histogram region
+    // the guess: its kGuessBins counters followed by the sample (kSampleSize
+    // keys); direct rows then reuse the region for the candidate histogram
+    // (kBins counters) and the selection (sel_cap pairs), the sample being dead
+    const size_t guess = static_cast<size_t>(kGuessBins) * 4 + static_cast<size_t>(kSampleSize) * 4;
     const size_t sel_bytes = static_cast<size_t>(sel_cap) * 8;
-    const size_t hist = sel_bytes > big_hist ? sel_bytes : big_hist;
+    size_t hist = sel_bytes > guess ? sel_bytes : guess;
+    if (hist < static_cast<size_t>(kBins) * 4) hist = static_cast<size_t>(kBins) * 4;
     if (width <= 2 * chunk) {
         pl.split = 0;
         pl.direct_max = static_cast<int32_t>(width);
@@ -102,8 +104,9 @@ int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *p
     pl.det_bytes = det_scratch_bytes(sel_cap);
     pl.row_smem_sorted = pl.off_stage + (stage > pl.det_bytes ? stage : pl.det_bytes);
     // split plans select nothing in the row kernel unless the output is
-    // sorted (short rows are written straight out): histogram and sample only
-    pl.row_smem = pl.split ? align_up(pl.off_hist + big_hist, 128) : pl.off_stage + stage;
+    // sorted (short rows are written straight out): the guess's counters and
+    // sample only (12 KB with the control block)
+    pl.row_smem = pl.split ? align_up(pl.off_hist + guess, 128) : pl.off_stage + stage;
     if (pl.row_smem_sorted > kMaxSmemBytes) return GBTOPK_EUNSUPPORTED;
     pl.ws_bytes = kWsHeaderBytes + static_cast<size_t>(num_rows) * pl.ws_row_bytes;
     *plan = pl;

@@ -896,7 +896,7 @@ __device__ void guess_from_sample(const uint32_t *sample, int m, int64_t n, int 
                                   int &bin_shift) {
     uint32_t r = guess_rank(n, k);
     if (r > static_cast<uint32_t>(m)) r = static_cast<uint32_t>(m);
-    t_lo = adaptive_threshold<NT, 512>(sample, m, r, kmin, kmax, hist, c);
+    t_lo = adaptive_threshold<NT, kGuessBins>(sample, m, r, kmin, kmax, hist, c);
     const int bits = 32 - __clz(kmax - t_lo);
     bin_shift = bits > kBinBits - 1 ? bits - (kBinBits - 1) : 0;
 }
@@ -1046,7 +1046,9 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
     Ctrl &c = *reinterpret_cast<Ctrl *>(smem);
     uint32_t *hist = reinterpret_cast<uint32_t *>(smem + p.plan.off_hist);
     uint2 *sel = reinterpret_cast<uint2 *>(smem + p.plan.off_hist);  // aliases hist
-    uint32_t *sample = reinterpret_cast<uint32_t *>(smem + p.plan.off_hist + kBins * 4);
+    // after the guess's counters; dead once the guess is made (direct rows
+    // then zero the whole histogram over it)
+    uint32_t *sample = reinterpret_cast<uint32_t *>(smem + p.plan.off_hist + kGuessBins * 4);
     uint8_t *stage = smem + p.plan.off_stage;  // direct rows; the sorted output's scratch
     const int64_t row = p.row0 + blockIdx.x;
     const int k = p.k;

@@ -318,6 +318,67 @@ def test_cuda_graph_replay_with_changing_lengths(dev):
         check_rows(logits, n, k, out, ref, vals)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("next_n", [1, 2, 3, 4])
+@pytest.mark.parametrize("cr", [1, 4])
+def test_graph_replay_mtp_grid_growing(dev, dtype, next_n, cr):
+    """16-bit logits, every next_n x compress_ratio pair, one captured CUDA
+    graph replayed over decode steps whose seq_lens grow by next_n, from
+    empty rows through the split pipeline to the width clamp."""
+    g = torch.Generator().manual_seed(700 + 10 * next_n + cr)
+    req, W, k = 4, 40000, 512
+    R = req * next_n
+    logits = torch.randn(R, W, generator=g)
+    x = logits.to(dtype).to(dev)
+    xc = x.cpu()
+    seq = torch.zeros(req, dtype=torch.int32, device=dev)
+    out = torch.empty(R, k, dtype=torch.int32, device=dev)
+    vals = torch.empty(R, k, dtype=dtype, device=dev)
+    s = torch.cuda.Stream(dev)
+    with torch.cuda.stream(s):
+        gb.top_k_varlen(x, seq, k, next_n=next_n, compress_ratio=cr, return_values=True,
+                        out_indices=out, out_values=vals)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            gb.top_k_varlen(x, seq, k, next_n=next_n, compress_ratio=cr, return_values=True,
+                            out_indices=out, out_values=vals)
+    start = torch.tensor([0, cr * k - 1, cr * 20000, cr * W - 2 * next_n], dtype=torch.int64)
+    for step in range(5):
+        lens = (start + step * next_n).to(torch.int32)
+        seq.copy_(lens)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        n = oracle.row_lengths(lens.tolist(), R, next_n, cr, W)
+        ref = _oracle_rows(xc, n, k, range(R))
+        check_rows(xc, n, k, out, ref, vals)
+
+
+@pytest.mark.parametrize("W", [1500, 10000, 100000])
+def test_back_to_back_with_a_producer(dev, W):
+    """Each call is a programmatic dependent of the kernel before it on the
+    stream: a producer rewrites the logits right before every call and right
+    after it, with no synchronisation; each call must see exactly the logits
+    written before it (small-row, single-block and split paths)."""
+    g = torch.Generator().manual_seed(900 + W)
+    R, k = 8, 512
+    srcs = [torch.randn(R, W, generator=g) for _ in range(3)]
+    srcs_d = [t.to(dev) for t in srcs]
+    seq = torch.randint(1, W + 1, (R,), generator=g, dtype=torch.int32)
+    seq[0] = W
+    x = torch.empty(R, W, device=dev)
+    outs = [torch.empty(R, k, dtype=torch.int32, device=dev) for _ in range(6)]
+    sd = seq.to(dev)
+    for i in range(6):
+        x.copy_(srcs_d[i % 3])            # the producer
+        gb.top_k_varlen(x, sd, k, out_indices=outs[i])
+    x.fill_(float("nan"))                 # a later writer must not reach the last call
+    torch.cuda.synchronize(dev)
+    n = oracle.row_lengths(seq.tolist(), R, 1, 1, W)
+    for i in range(6):
+        src = srcs[i % 3]
+        check_rows(src, n, k, outs[i], _oracle_rows(src, n, k, range(R)))
+
+
 # ------------------------------------------------------------------ page table
 
 def _run_page_table(dev, c, det=None, rows=None, with_raw=True, prs=True, pt_view=None):
