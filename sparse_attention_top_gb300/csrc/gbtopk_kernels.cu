@@ -38,6 +38,11 @@
 
 namespace gbtopk {
 
+// Trace rows of each kernel's blocks (GBTOPK_TRACE builds): row kernel from 0,
+// stream kernel from kTraceStream, finalize kernel from kTraceFinal.
+constexpr int kTraceStream = 32768;
+constexpr int kTraceFinal = 40960;
+
 #ifdef GBTOPK_TRACE
 // Phase timestamps (%globaltimer, ns) of the first kTraceBlocks blocks, for
 // builds compiled with -DGBTOPK_TRACE (read back by gbtopk_trace_read).
@@ -83,7 +88,6 @@ struct Elem<0> {  // fp32
     static constexpr int kBytes = 4;
     static constexpr int kKeyBits = 32;
     static constexpr uint32_t kLowest = 0xFF7FFFFFu;   // -FLT_MAX
-    static constexpr uint32_t kKeyZeroRaw = 0xFFFFFFFFu; // a raw whose key is 0
     __device__ __forceinline__ static uint32_t key(uint32_t u) {
         u = (u == 0x80000000u) ? 0u : u;
         return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
@@ -94,7 +98,6 @@ struct Elem16 {
     using raw_t = uint16_t;
     static constexpr int kBytes = 2;
     static constexpr int kKeyBits = 16;
-    static constexpr uint32_t kKeyZeroRaw = 0xFFFFu;
     __device__ __forceinline__ static uint32_t key(uint32_t u) {
         u &= 0xFFFFu;
         u = (u == 0x8000u) ? 0u : u;
@@ -324,28 +327,6 @@ struct PairSrc {  // (raw, column) pairs in shared memory
         raw = v.x;
         key = Elem<DT>::key(v.x);
         idx = v.y;
-    }
-};
-
-template <int DT>
-struct GlobalPairSrc {  // (raw, column) pairs published by other blocks (read from L2)
-    static constexpr int kBatch = 8;
-    const uint2 *p;
-    __device__ __forceinline__ void get(int64_t i, uint32_t &key, uint32_t &idx, uint32_t &raw) const {
-        const uint2 v = __ldcg(p + i);
-        raw = v.x;
-        key = Elem<DT>::key(v.x);
-        idx = v.y;
-    }
-};
-
-struct KeyArraySrc {  // keys already mapped (the row sample)
-    static constexpr int kBatch = 8;
-    const uint32_t *k;
-    __device__ __forceinline__ void get(int64_t i, uint32_t &key, uint32_t &idx, uint32_t &raw) const {
-        key = k[i];
-        idx = static_cast<uint32_t>(i);
-        raw = 0;
     }
 };
 
@@ -645,7 +626,7 @@ __device__ void emit_sorted_impl(const Params &p, int64_t row, const uint2 *sel,
         kmax = key > kmax ? key : kmax;
     }
     block_minmax(kmin, kmax, c);
-    if (NT == kFinalThreads && tid == 0) GBTOPK_TRACE_SET(40960 + blockIdx.x, 3, -1);
+    if (NT == kFinalThreads && tid == 0) GBTOPK_TRACE_SET(kTraceFinal + blockIdx.x, 3, -1);
     kmin = c.key_min;
     const int bits = 32 - __clz(c.key_max - kmin);
     const int shift = bits > kBinBits ? bits - kBinBits : 0;
@@ -654,7 +635,7 @@ __device__ void emit_sorted_impl(const Params &p, int64_t row, const uint2 *sel,
     __syncthreads();
     // bins[b] = pairs in the bins above b
     scan_from_top<NT, kBins>(bins, c, [&](uint32_t b, uint32_t above, uint32_t) { bins[b] = above; });
-    if (NT == kFinalThreads && tid == 0) GBTOPK_TRACE_SET(40960 + blockIdx.x, 4, -1);
+    if (NT == kFinalThreads && tid == 0) GBTOPK_TRACE_SET(kTraceFinal + blockIdx.x, 4, -1);
     for (int i = tid; i < m; i += NT) {
         const uint2 v = sel[i];
         const uint32_t at = atomicAdd(&bins[(Elem<DT>::key(v.x) - kmin) >> shift], 1u);
@@ -662,7 +643,7 @@ __device__ void emit_sorted_impl(const Params &p, int64_t row, const uint2 *sel,
         if constexpr (!Compact) comp[at] = sort_composite<DT>(v);
     }
     __syncthreads();
-    if (NT == kFinalThreads && tid == 0) GBTOPK_TRACE_SET(40960 + blockIdx.x, 5, -1);
+    if (NT == kFinalThreads && tid == 0) GBTOPK_TRACE_SET(kTraceFinal + blockIdx.x, 5, -1);
     // bins[b] now ends b's segment, which starts where b + 1's ends
     if constexpr (Compact) {
         // rank and write in one pass (no room for an inverse map)
@@ -689,7 +670,7 @@ __device__ void emit_sorted_impl(const Params &p, int64_t row, const uint2 *sel,
             inv[lo + before] = pos[j];
         }
         __syncthreads();
-        if (NT == kFinalThreads && tid == 0) GBTOPK_TRACE_SET(40960 + blockIdx.x, 8, -1);
+        if (NT == kFinalThreads && tid == 0) GBTOPK_TRACE_SET(kTraceFinal + blockIdx.x, 8, -1);
 #pragma unroll 4
         for (int j = tid; j < m; j += NT) {
             const uint2 v = sel[inv[j]];
@@ -1276,7 +1257,7 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
     StageMeta *meta = reinterpret_cast<StageMeta *>(smem + kCtrlBytes - kStages * sizeof(StageMeta));
     uint8_t *stages = smem + p.plan.stream_smem - static_cast<size_t>(kStages) * kStageBytes;
     const int64_t CH = p.plan.chunk;
-    constexpr int kTraceBase = 32768;
+    constexpr int kTraceBase = kTraceStream;
     (void)kTraceBase;
     GBTOPK_TRACE_POINT(0, 0);
 
@@ -1690,7 +1671,7 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
     const bool sorted = sorted_output(p.deterministic);
     const int tie = tie_mode(p.deterministic);
     const int tid = threadIdx.x;
-    constexpr int kTraceBase = 40960;
+    constexpr int kTraceBase = kTraceFinal;
     (void)kTraceBase;
     int64_t n, col0;
     row_window(p, row, n, col0);
