@@ -209,6 +209,15 @@ def oracle_rows_per_s(case, seconds: float = 10.0, rows_per_step: int = 8):
     return done / dt, done, dt
 
 
+def workload_config(args, case) -> dict:
+    """The workload keys of the JSON line's config, shared by both arms."""
+    R, W = case.logits.shape
+    hinted = case.pre_idx is not None
+    return {"workload": f"{args.workload}: {R} rows x {W} fp32, top_k={case.top_k}, "
+                        f"seq_lens {SEQ_DIST[args.workload](W)}, hint={'yes' if hinted else 'no'}",
+            "rows": R, "width": W, "top_k": case.top_k, "hinted": hinted}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -239,7 +248,7 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "rows/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": {"workload": args.workload, "rows_per_step": rows_per_step},
+            "data": "synthetic", "config": workload_config(args, case),
             "cpu_baseline": {"value": v, "unit": "rows/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0,
@@ -359,10 +368,7 @@ def run_gbtopk(args, rank, world, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": f"{args.workload}: {R} rows x {W} fp32, top_k={k}, "
-                                   f"seq_lens {SEQ_DIST[args.workload](W)}, "
-                                   f"hint={'yes' if hint_d else 'no'}",
-                       "rows": R, "width": W, "top_k": k, "hinted": hint_d is not None,
+            "config": {**workload_config(args, case),
                        "l2": f"inputs rotate over {copies} device copies "
                              f"({copies * valid_bytes / 2**20:.0f} MB valid > L2)",
                        "parallelism": f"replicas x{world} (rows independent)"},
