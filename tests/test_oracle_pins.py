@@ -352,3 +352,24 @@ def test_large_ties_brute_force(oracle_mod):
         keep = sorted(range(n), key=lambda j: (-vals[j], -j))[:k]
         want = sorted(keep, key=lambda j: (-vals[j], j)) + [-1] * (k - min(k, n))
         assert idx[0].tolist() == want, (vals[:n], k)
+
+
+@pytest.mark.parametrize("k", [4096, 16384])
+def test_large_k_brute_force(oracle_mod, k):
+    """top_k beyond 2048 (up to 16384): the oracle's selection, the SMALL and
+    LARGE tie modes and the padding against pure Python sorts of rows with
+    heavy ties, rows longer and shorter than k."""
+    rnd = random.Random(k)
+    for n in (k - 1, k, k + 1, 20000):
+        vals = [float(rnd.randint(-40, 40)) / 8 for _ in range(n)]
+        row = torch.tensor(vals, dtype=torch.float32)
+        idx, _ = oracle_mod.select_row(row, n, k)
+        assert idx.tolist() == _brute(vals, n, k), (k, n)
+        small, _ = oracle_mod.topk_varlen_ties(row.view(1, -1), torch.tensor([n], dtype=torch.int32),
+                                               k, False)
+        assert small[0].tolist() == _brute(vals, n, k), (k, n)
+        large, _ = oracle_mod.topk_varlen_ties(row.view(1, -1), torch.tensor([n], dtype=torch.int32),
+                                               k, True)
+        keep = sorted(range(n), key=lambda j: (-vals[j], -j))[:k]
+        want = sorted(keep, key=lambda j: (-vals[j], j)) + [-1] * (k - min(k, n))
+        assert large[0].tolist() == want, (k, n)
