@@ -129,6 +129,9 @@ def gbtopk_workspace_bytes(num_rows: int, width: int, top_k: int, dtype: torch.d
 
 
 def gbtopk_plan_query(num_rows: int, width: int, top_k: int, dtype: torch.dtype) -> dict:
+    """The launch plan of a geometry (chunking, shared-memory sizes per kernel,
+    workspace bytes), as the library computes it; raises GbtopkError when the
+    geometry is refused."""
     out = (ctypes.c_int64 * 11)()
     _check(load_library().gbtopk_plan_query(num_rows, width, top_k, _DTYPES[dtype], out))
     keys = ["chunk", "chunks_per_row", "direct_max", "row_smem", "split", "row_candidates",
