@@ -709,3 +709,70 @@ def test_large_top_k_page_table(dev):
     c = workloads.page_table_case(rows=32, width=32768, row_stride=33024, page_size=64,
                                   pt_cols=1024, top_k=8192, seed=5099)
     _run_page_table(dev, c)
+
+
+def _windows(scores, lengths, starts):
+    """Each page-table row's valid window, left-aligned, and its length."""
+    R, W = scores.shape
+    n = [oracle.ragged_length(int(lengths[r]), int(starts[r]), W) for r in range(R)]
+    win = torch.zeros(R, W, dtype=scores.dtype)
+    for r in range(R):
+        win[r, :n[r]] = scores[r, int(starts[r]):int(starts[r]) + n[r]]
+    return win, n
+
+
+@pytest.mark.parametrize("k", [2048, 4096])
+def test_page_table_tie_large_sorted(dev, k):
+    """The compact page-table transform with LARGE ties and the sorted order:
+    out_raw is exactly the oracle's LARGE selection over each row's window
+    (canonical order) and out its page-table translation."""
+    c = workloads.page_table_case(rows=24, width=32768, row_stride=33024, page_size=64,
+                                  pt_cols=1024, top_k=k, seed=5111)
+    scores = torch.round(c.scores * 4) / 4                     # heavy ties
+    R, W = scores.shape
+    raw = torch.empty(R, k, dtype=torch.int32, device=dev)
+    out, _ = gb.top_k_page_table_transform(
+        scores.to(dev), c.lengths.to(dev), c.page_table.to(dev), k, c.page_size,
+        c.row_starts.to(dev), c.page_table_row_starts.to(dev), out_raw_indices=raw,
+        deterministic=True, tie_mode="large")
+    torch.cuda.synchronize(dev)
+    win, n = _windows(scores, c.lengths, c.row_starts)
+    ref, _ = oracle.topk_varlen_ties(win, torch.tensor(n, dtype=torch.int32), k, True,
+                                     return_values=False)
+    assert torch.equal(raw.cpu(), ref)
+    o = out.cpu()
+    for r in range(R):
+        start = int(c.page_table_row_starts[r])
+        for j, idx in enumerate(ref[r].tolist()):
+            if idx < 0:
+                assert int(o[r, j]) == -1
+            else:
+                page = int(c.page_table[r, start + idx // c.page_size])
+                assert int(o[r, j]) == page * c.page_size + idx % c.page_size
+
+
+def test_page_table_cu_seqlens_tie_large(dev):
+    """The per-request page table (page_size 1) with LARGE ties at top_k 4096:
+    decoded back to columns, each row's set is the oracle's LARGE selection."""
+    R, W, k = 30, 50000, 4096
+    scores, lengths, starts = _ragged_case(R, W, 7300)
+    scores = torch.round(scores * 2) / 2                       # heavy ties
+    g = torch.Generator().manual_seed(13)
+    cu = torch.tensor([0, 7, 7, 19, 30], dtype=torch.int32)
+    B = cu.numel() - 1
+    pt = torch.stack([torch.randperm(W, generator=g) + b * 10_000_000 for b in range(B)]).to(torch.int32)
+    out = gb.top_k_page_table_transform_cu_seqlens(
+        scores.to(dev), lengths.to(dev), pt.to(dev), cu.to(dev), k, row_starts=starts.to(dev),
+        tie_mode="large")
+    torch.cuda.synchronize(dev)
+    win, n = _windows(scores, lengths, starts)
+    ref, _ = oracle.topk_varlen_ties(win, torch.tensor(n, dtype=torch.int32), k, True,
+                                     return_values=False)
+    o = out.cpu()
+    for r in range(R):
+        b = next(q for q in range(B) if int(cu[q]) <= r < int(cu[q + 1]))
+        inv = {int(v): j for j, v in enumerate(pt[b].tolist())}
+        m = min(k, n[r])
+        assert int((o[r] == -1).sum()) == k - m, f"row {r}: -1 count"
+        got = sorted(inv[int(v)] for v in o[r].tolist() if v != -1)
+        assert got == sorted(ref[r][:m].tolist()), f"row {r}: selected set differs"
