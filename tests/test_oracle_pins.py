@@ -136,10 +136,13 @@ def golden_failures(lib):
         lengths = torch.tensor(case["lengths"], dtype=torch.int32)
         cu = torch.tensor(case["cu_seqlens_q"], dtype=torch.int32)
         pt = torch.tensor(case["page_table"], dtype=torch.int32)
+        rs = (torch.tensor(case["row_starts"], dtype=torch.int32) if case.get("row_starts") is not None
+              else None)
         k = case["k"]
         out = torch.empty(R, k, dtype=torch.int32)
         rc = lib.oracle_seqs_page_table_transform(
-            scores.data_ptr(), 0, R, W, W, lengths.data_ptr(), None, pt.data_ptr(), pt.shape[1],
+            scores.data_ptr(), 0, R, W, W, lengths.data_ptr(),
+            rs.data_ptr() if rs is not None else None, pt.data_ptr(), pt.shape[1],
             pt.shape[1], cu.data_ptr(), cu.numel() - 1, k, out.data_ptr())
         if rc != 0 or out.tolist() != case["out"]:
             fails.append(f"requests {case['name']}: rc={rc} {out.tolist()}")
@@ -286,6 +289,10 @@ MUTANTS = [
     ("large ties keep the small columns", "return (x->j > y->j) ? -1 : (x->j < y->j ? 1 : 0);",
      "return (x->j < y->j) ? -1 : (x->j > y->j ? 1 : 0);"),
     ("large ties left unsorted", "        qsort(items, (size_t)m, sizeof(item_t), by_value_desc_index_asc);\n", ""),
+    ("window not clamped to the width", "return len < room ? len : room;", "return len;"),
+    ("start outside the width not empty", "if (row_start < 0 || row_start > width || len <= 0)",
+     "if (len <= 0)"),
+    ("page column outside the table kept", "if (col < 0 || col >= pt_cols) {", "if (0) {"),
 ]
 
 
