@@ -223,13 +223,18 @@ int gbtopk_device_status(void *workspace, uint32_t *flags, void *stream);
 
 /*
  * gbtopk_plan_query — the launch plan for a geometry, for inspection and
- * tests.  Fills out[0..10] = {columns per stream chunk, chunks of the widest
- * split row (1 when no row is split), longest row finished by the one-block
- * row kernel, row-kernel shared memory bytes, split (0/1), candidate entries
- * reserved per split row, stream-kernel shared memory bytes, finalize-kernel
- * shared memory bytes, workspace bytes, workspace bytes per row, row-kernel
- * shared memory bytes with GBTOPK_SORTED}.  Returns GBTOPK_OK or
- * GBTOPK_EINVAL / GBTOPK_EUNSUPPORTED.
+ * tests.  `out` must hold 13 entries: out[0..12] = {columns per chunk of a
+ * split row, chunks of the widest split row (1 when no row is split),
+ * longest row finished by the one-block row kernel, row-kernel shared
+ * memory bytes, split (0/1), candidate entries reserved per split row,
+ * stream-kernel shared memory bytes (0 unless split rows take the three-
+ * kernel path), finalize-kernel shared memory bytes (likewise), workspace
+ * bytes, workspace bytes per row, row-kernel shared memory bytes with
+ * GBTOPK_SORTED, fused (1 when split rows take the two-kernel path: the
+ * row kernel's guess, then one chunk-kernel block per chunk, the row's last
+ * block selecting it), chunk-kernel shared memory bytes (fused plans)}.
+ * Returns GBTOPK_OK or GBTOPK_EINVAL / GBTOPK_EUNSUPPORTED (nothing is
+ * written then).
  */
 int gbtopk_plan_query(int64_t num_rows, int64_t width, int32_t top_k, int dtype,
                       int64_t *out);

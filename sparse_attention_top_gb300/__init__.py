@@ -132,10 +132,11 @@ def gbtopk_plan_query(num_rows: int, width: int, top_k: int, dtype: torch.dtype)
     """The launch plan of a geometry (chunking, shared-memory sizes per kernel,
     workspace bytes), as the library computes it; raises GbtopkError when the
     geometry is refused."""
-    out = (ctypes.c_int64 * 11)()
+    out = (ctypes.c_int64 * 13)()
     _check(load_library().gbtopk_plan_query(num_rows, width, top_k, _DTYPES[dtype], out))
     keys = ["chunk", "chunks_per_row", "direct_max", "row_smem", "split", "row_candidates",
-            "stream_smem", "final_smem", "workspace_bytes", "ws_row_bytes", "row_smem_sorted"]
+            "stream_smem", "final_smem", "workspace_bytes", "ws_row_bytes", "row_smem_sorted",
+            "fused", "fused_smem"]
     return dict(zip(keys, list(out)))
 
 

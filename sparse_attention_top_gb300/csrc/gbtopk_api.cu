@@ -30,9 +30,12 @@ bool overlaps(const void *a, size_t an, const void *b, size_t bn) {
 //
 // Rows of up to direct_max columns are finished by the row kernel alone
 // (one block per row, the row staged in shared memory).  When the width
-// allows longer rows, those are split into chunks of kChunkBytes and run
-// through three kernels: the row kernel (threshold guess), the persistent
-// stream kernel (filter every chunk) and the finalize kernel (exact select).
+// allows longer rows, those are split into chunks.  With top_k up to
+// kPairSortMax the split rows run through two kernels: the row kernel
+// (threshold guess) and the chunk kernel (one block per kFusedChunkBytes
+// chunk, the row's last block selecting the row).  Larger top_k takes three:
+// the row kernel, the persistent stream kernel (kChunkBytes chunks) and the
+// finalize kernel, which has room for the larger selection.
 int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *plan) {
     if (num_rows < 0 || width < 0 || top_k < 1 ||
         (dtype != GBTOPK_F32 && dtype != GBTOPK_BF16 && dtype != GBTOPK_F16))
@@ -57,6 +60,30 @@ int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *p
         pl.split = 0;
         pl.direct_max = static_cast<int32_t>(width);
         pl.chunks_per_row = 1;
+    } else if (sel_cap <= kPairSortMax &&
+               num_rows * ((width + kFusedChunkBytes / es - 1) / (kFusedChunkBytes / es)) <= kFusedMaxSlots) {
+        // every row longer than top_k: row kernel guess, then one chunk
+        // kernel block per kFusedChunkBytes of the row
+        pl.split = 1;
+        pl.fused = 1;
+        pl.direct_max = top_k;
+        const int64_t fchunk = kFusedChunkBytes / es;
+        pl.chunk = static_cast<int32_t>(fchunk);
+        pl.chunks_per_row = static_cast<int32_t>((width + fchunk - 1) / fchunk);
+        if (pl.chunks_per_row > kThreads) return GBTOPK_EUNSUPPORTED;
+        pl.block_rows = num_rows;
+        pl.fused_smem = kCtrlBytes + kFusedStageBytes;
+        pl.final_sel_bytes = static_cast<size_t>(kPairSortMax) * 8;
+        int64_t entries = 0;
+        for (int64_t j = 1; j <= pl.chunks_per_row; ++j) {
+            int64_t n_min = (j - 1) * fchunk + 1;
+            if (n_min <= pl.direct_max) n_min = pl.direct_max + 1;
+            if (n_min > width || n_min > j * fchunk) continue;
+            const int64_t e = j * static_cast<int64_t>(chunk_seg_cap(n_min, top_k, pl.chunk));
+            entries = e > entries ? e : entries;
+        }
+        pl.row_seg_entries = entries;
+        pl.ws_row_bytes = align_up(ws_seg_offset(pl.chunks_per_row) + 8 * static_cast<size_t>(entries), 256);
     } else {
         // every row longer than top_k runs through the split pipeline
         pl.split = 1;
@@ -75,7 +102,7 @@ int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *p
                                  ? static_cast<size_t>(sel_cap) * 8
                                  : static_cast<size_t>(kFinalHistBytes);
         const size_t fixed = kCtrlBytes + pl.final_sel_bytes + static_cast<size_t>(kFinalBCap) * 8 +
-                             4 * static_cast<size_t>(kFinalThreads);
+                             4 * static_cast<size_t>(kFinalThreads) + 4 * static_cast<size_t>(kCoarseBins);
         size_t gather = static_cast<size_t>(kGatherCandidates) * 8;
         if (fixed + gather > kMaxSmemBytes) gather = kMaxSmemBytes > fixed ? (kMaxSmemBytes - fixed) / 16 * 16 : 0;
         if (gather < det_scratch_bytes(sel_cap)) return GBTOPK_EUNSUPPORTED;
@@ -92,8 +119,7 @@ int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *p
             entries = e > entries ? e : entries;
         }
         pl.row_seg_entries = entries;
-        const size_t seg_off = align_up(kRowInfoBytes + 4 * static_cast<size_t>(pl.chunks_per_row), 16);
-        pl.ws_row_bytes = align_up(seg_off + 8 * static_cast<size_t>(entries), 256);
+        pl.ws_row_bytes = align_up(ws_seg_offset(pl.chunks_per_row) + 8 * static_cast<size_t>(entries), 256);
     }
     // the row kernel stages direct rows only in plans without a split
     // pipeline; the sorted output's scratch reuses the stage (free once the
@@ -336,6 +362,8 @@ int gbtopk_plan_query(int64_t num_rows, int64_t width, int32_t top_k, int dtype,
     out[8] = static_cast<int64_t>(plan.ws_bytes);
     out[9] = static_cast<int64_t>(plan.ws_row_bytes);
     out[10] = static_cast<int64_t>(plan.row_smem_sorted);
+    out[11] = plan.fused;
+    out[12] = static_cast<int64_t>(plan.fused_smem);
     return GBTOPK_OK;
 }
 

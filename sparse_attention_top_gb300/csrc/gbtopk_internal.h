@@ -31,8 +31,33 @@ constexpr int kGatherCandidates = 8192; // candidates the finalize kernel gather
 constexpr size_t kMaxSmemBytes = 232448;  // dynamic shared memory one block may opt into (227 KB)
 constexpr int kPairSortMax = 2048;     // sorted output copies up to this many pairs, else 16-bit positions
 constexpr size_t kWsHeaderBytes = 256; // device status word + padding
-constexpr size_t kRowInfoBytes = 16;   // t_lo, bin shift (written by the row kernel)
+constexpr size_t kRowInfoBytes = 16;   // t_lo, bin shift, chunk ticket (written by the row kernel)
 constexpr uint32_t kSpinLimit = 1u << 22;
+// Coarse candidate bins of a split row's final selection: bin_of's bins
+// taken kCoarseShift bits at a time, the top bin open-ended.
+constexpr int kCoarseBins = 256;
+constexpr int kCoarseShift = 4;
+
+// Fused split path (top_k <= kPairSortMax): one block of kThreads per chunk
+// of kFusedChunkBytes, finalized in its own shared memory by the row's last
+// block.  The finalize regions inside the chunk's stage (byte offsets):
+// boundary list, chunk offsets, coarse-bin slot counters, gathered
+// candidates, and the selection (up to kPairSortMax pairs) at the end; the
+// sorted-output scratch reuses everything before the selection once the row
+// is selected.
+constexpr int kFusedChunkBytes = 65536;
+constexpr int kFusedStageBytes = kFusedChunkBytes + 32;
+constexpr int kFusedBCap = 256;
+constexpr int kFusedOffChOff = kFusedBCap * 8;
+constexpr int kFusedOffFill = kFusedOffChOff + kThreads * 4;
+constexpr int kFusedOffCand = kFusedOffFill + kCoarseBins * 4;
+constexpr int kFusedOffSel = kFusedStageBytes - kPairSortMax * 8;
+constexpr int kFusedGatherCap = (kFusedOffSel - kFusedOffCand) / 16 * 2;
+// The fused path serves batches of up to kFusedMaxSlots (row, chunk) slots:
+// about four waves of three chunk blocks per SM.  Larger batches stream
+// through the persistent kernel's ring, which keeps every SM's copies in
+// flight while its consumers filter.
+constexpr int64_t kFusedMaxSlots = 2048;
 
 // Flags of Params::deterministic (the public GBTOPK_SORTED / GBTOPK_TIE_*).
 constexpr int kSortedFlag = 1;
@@ -48,9 +73,11 @@ __host__ __device__ inline bool sorted_output(int flags) { return (flags & kSort
 
 // Bits of the device status word.
 constexpr uint32_t kStatusWaitTimeout = 1u;
+constexpr uint32_t kStatusCopyLost = 2u;  // a bulk copy never completed: outputs unreliable
 
 struct Plan {
-    int32_t chunk;           // elements per stream chunk
+    int32_t fused;           // 1: split rows run through the chunk kernel (row guess + chunk kernel)
+    int32_t chunk;           // elements per chunk of a split row
     int32_t direct_max;      // rows up to this length are finished by the row kernel
     int32_t chunks_per_row;  // chunks of the widest split row (0: no split rows possible)
     int32_t split;           // 1 when some row can exceed direct_max
@@ -61,6 +88,7 @@ struct Plan {
     int32_t stream_grid;     // persistent stream blocks
     int64_t row_seg_entries; // candidate entries reserved per split row
     size_t row_smem, stream_smem, final_smem;
+    size_t fused_smem;       // chunk kernel (fused plans)
     size_t off_hist, off_stage;  // row kernel layout
     size_t ws_row_bytes;     // per-row workspace bytes (split plans)
     size_t ws_bytes;         // total workspace bytes
@@ -105,6 +133,17 @@ __host__ __device__ inline uint32_t guess_rank(int64_t n, int32_t k) {
     float r = ceilf(e + 6.0f * sqrtf(e) + 2.0f);
     if (r > static_cast<float>(kSampleSize)) r = static_cast<float>(kSampleSize);
     return static_cast<uint32_t>(r);
+}
+
+// Byte offsets inside a split row's workspace block: the row info, one
+// count per chunk, the row's coarse candidate histogram (kCoarseBins
+// counters, zeroed by the row kernel, counted by the chunk kernel), then
+// the chunk segments.
+__host__ __device__ inline size_t ws_hist_offset(int32_t chunks_per_row) {
+    return (kRowInfoBytes + 4 * static_cast<size_t>(chunks_per_row) + 15) / 16 * 16;
+}
+__host__ __device__ inline size_t ws_seg_offset(int32_t chunks_per_row) {
+    return ws_hist_offset(chunks_per_row) + static_cast<size_t>(kCoarseBins) * 4;
 }
 
 // Candidate capacity of one chunk of a split row with n valid columns (1.5x

@@ -29,6 +29,9 @@
 // Ranking uses order-preserving integer keys (signed zeros equal; +-inf and
 // denormals exact), so no float compare depends on flush-to-zero.
 #include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -42,6 +45,7 @@ namespace gbtopk {
 // stream kernel from kTraceStream, finalize kernel from kTraceFinal.
 constexpr int kTraceStream = 32768;
 constexpr int kTraceFinal = 40960;
+constexpr int kTraceChunk = 8192;  // chunk kernel blocks (up to 24576 of them)
 
 #ifdef GBTOPK_TRACE
 // Phase timestamps (%globaltimer, ns) of the first kTraceBlocks blocks, for
@@ -580,6 +584,7 @@ __device__ __forceinline__ void put_slot(const Params &p, int64_t row, const Row
 template <int DT>
 __device__ void emit(const Params &p, int64_t row, const uint2 *sel, int m) {
     const RowEpi ep = row_epilogue(p, row);
+#pragma unroll 4
     for (int j = threadIdx.x; j < p.k; j += blockDim.x) {
         const bool live = j < m;
         put_slot<DT>(p, row, ep, j, live ? static_cast<int32_t>(sel[j].y) : -1, live ? sel[j].x : 0u);
@@ -745,6 +750,13 @@ __device__ __forceinline__ uint32_t bin_of(uint32_t key, uint32_t t_lo, int bin_
     return b < static_cast<uint32_t>(kBins - 1) ? b : static_cast<uint32_t>(kBins - 1);
 }
 
+// Coarse bin of a candidate key (kCoarseShift bits of bin_of at a time; the
+// top bin takes everything above).
+__device__ __forceinline__ uint32_t coarse_bin(uint32_t key, uint32_t t_lo, int bin_shift) {
+    const uint32_t b = (key - t_lo) >> (bin_shift + kCoarseShift);
+    return b < static_cast<uint32_t>(kCoarseBins - 1) ? b : static_cast<uint32_t>(kCoarseBins - 1);
+}
+
 __device__ __forceinline__ float float_of_key(uint32_t t) {
     return __uint_as_float((t & 0x80000000u) ? (t & 0x7FFFFFFFu) : ~t);
 }
@@ -835,10 +847,55 @@ __device__ void find_bin_from_top(const uint32_t *hist, uint32_t r, Ctrl &c) {
 // bins, so the shared-memory increments rarely collide) finds the bin that
 // holds the r-th largest key; a second round splits that bin into NB
 // sub-bins.  Returns the lower key edge of the sub-bin holding the r-th
-// largest key, so at least r keys are >= the result.
+// largest key, so at least r keys are >= the result.  Also returns, in
+// `upper_e`, the top key of the first-round bin holding the e-th largest
+// key (1 <= e <= r): an upper estimate of that key.
+// Warp 0: for ranks r0 and r1 (1-based, <= the total count), the bins of
+// hist[NB] holding the r0-th and r1-th largest items: c.bcast[2 + 3i] = the
+// bin, c.bcast[3 + 3i] = the count above it, c.bcast[4 + 3i] = its count
+// (i = 0, 1).  Lane l holds bins NB - 1 - (NB / 32) l - j.  The caller syncs
+// the block after it.
+template <int NB>
+__device__ __forceinline__ void warp_find_two_bins(const uint32_t *hist, uint32_t r0, uint32_t r1, Ctrl &c) {
+    constexpr int PER = NB / 32;
+    if (threadIdx.x >= 32) return;
+    const uint32_t lane = lane_id();
+    uint32_t cnt[PER], s = 0;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        cnt[j] = hist[NB - 1 - PER * static_cast<int>(lane) - j];
+        s += cnt[j];
+    }
+    uint32_t incl = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= static_cast<uint32_t>(off)) incl += y;
+    }
+    const uint32_t excl = incl - s;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint32_t r = i == 0 ? r0 : r1;
+        const uint32_t bal = __ballot_sync(0xffffffffu, excl < r && r <= incl);
+        if (bal != 0u && static_cast<int>(lane) == __ffs(bal) - 1) {
+            uint32_t acc = excl;
+#pragma unroll
+            for (int j = 0; j < PER; ++j) {
+                if (acc + cnt[j] >= r) {
+                    c.bcast[2 + 3 * i] = static_cast<uint32_t>(NB - 1 - PER * static_cast<int>(lane) - j);
+                    c.bcast[3 + 3 * i] = acc;
+                    c.bcast[4 + 3 * i] = cnt[j];
+                    break;
+                }
+                acc += cnt[j];
+            }
+        }
+    }
+}
+
 template <int NT, int NB>
-__device__ uint32_t adaptive_threshold(const uint32_t *keys, int m, uint32_t r, uint32_t kmin,
-                                       uint32_t kmax, uint32_t *hist, Ctrl &c) {
+__device__ uint32_t adaptive_threshold(const uint32_t *keys, int m, uint32_t r, uint32_t e, uint32_t kmin,
+                                       uint32_t kmax, uint32_t *hist, Ctrl &c, uint32_t &upper_e) {
     constexpr int NBITS = NB == 512 ? 9 : (NB == 1024 ? 10 : (NB == 2048 ? 11 : 12));
     static_assert((1 << NBITS) == NB, "bin count");
     const int bits = 32 - __clz(kmax - kmin);
@@ -848,13 +905,16 @@ __device__ uint32_t adaptive_threshold(const uint32_t *keys, int m, uint32_t r, 
     __syncthreads();
     for (int i = threadIdx.x; i < m; i += NT) atomicAdd(&hist[(keys[i] - kmin) >> shift], 1u);
     __syncthreads();
-    find_bin_from_top<NT, NB>(hist, r, c);
-    const uint32_t b = c.bcast[2];
-    const uint32_t rem = r - c.bcast[3];
-    const uint32_t edge = kmin + (b << shift);
-    if (shift == 0 || c.bcast[4] == rem) return edge;  // exact key, or the whole bin is needed
-    const int shift2 = shift > NBITS ? shift - NBITS : 0;
+    warp_find_two_bins<NB>(hist, e, r, c);
     __syncthreads();
+    const uint32_t be = c.bcast[2];
+    upper_e = kmin + (be << shift) + ((1u << shift) - 1u);
+    if (upper_e < kmin || upper_e > kmax) upper_e = kmax;  // the top bin may reach past kmax
+    const uint32_t b = c.bcast[5];
+    const uint32_t rem = r - c.bcast[6];
+    const uint32_t edge = kmin + (b << shift);
+    if (shift == 0 || c.bcast[7] == rem) return edge;  // exact key, or the whole bin is needed
+    const int shift2 = shift > NBITS ? shift - NBITS : 0;
 #pragma unroll
     for (int j = 0; j < NB / NT; ++j) hist[threadIdx.x + j * NT] = 0;
     __syncthreads();
@@ -863,22 +923,30 @@ __device__ uint32_t adaptive_threshold(const uint32_t *keys, int m, uint32_t r, 
         if ((d >> shift) == b) atomicAdd(&hist[(d - (b << shift)) >> shift2], 1u);
     }
     __syncthreads();
-    find_bin_from_top<NT, NB>(hist, rem, c);
+    warp_find_two_bins<NB>(hist, rem, rem, c);
+    __syncthreads();
     return edge + (c.bcast[2] << shift2);
 }
 
 // The guess from a sample of m keys (with their min and max) of a row of n
 // columns: t_lo such that, with high probability, at least k row elements
 // are >= t_lo (the sample rank r = e + 6 sqrt(e) + 2, e = m k / n); and the
-// histogram scale mapping keys t_lo .. key_max onto the lower half of kBins.
+// histogram scale of the candidates: keys t_lo .. t_est map onto the lower
+// half of kBins, t_est being an upper estimate of the sample's e-th key
+// (where the k-th key of the row is expected), so the k-th key lands in
+// fine bins even when the keys above it span many binades or both signs;
+// keys far above it pile into the top bins, which are taken whole.
 template <int NT>
 __device__ void guess_from_sample(const uint32_t *sample, int m, int64_t n, int k, uint32_t kmin,
                                   uint32_t kmax, uint32_t *hist, Ctrl &c, uint32_t &t_lo,
                                   int &bin_shift) {
     uint32_t r = guess_rank(n, k);
     if (r > static_cast<uint32_t>(m)) r = static_cast<uint32_t>(m);
-    t_lo = adaptive_threshold<NT, kGuessBins>(sample, m, r, kmin, kmax, hist, c);
-    const int bits = 32 - __clz(kmax - t_lo);
+    uint32_t e = static_cast<uint32_t>((static_cast<int64_t>(m) * k + n - 1) / n);
+    e = e < 1u ? 1u : (e > r ? r : e);
+    uint32_t t_est;
+    t_lo = adaptive_threshold<NT, kGuessBins>(sample, m, r, e, kmin, kmax, hist, c, t_est);
+    const int bits = 32 - __clz(t_est - t_lo);
     bin_shift = bits > kBinBits - 1 ? bits - (kBinBits - 1) : 0;
 }
 
@@ -1001,9 +1069,11 @@ __device__ __forceinline__ uint32_t *row_info(const Params &p, int64_t row) {
 __device__ __forceinline__ uint32_t *row_counts(const Params &p, int64_t row) {
     return reinterpret_cast<uint32_t *>(row_ws(p, row) + kRowInfoBytes);
 }
+__device__ __forceinline__ uint32_t *row_hist(const Params &p, int64_t row) {
+    return reinterpret_cast<uint32_t *>(row_ws(p, row) + ws_hist_offset(p.plan.chunks_per_row));
+}
 __device__ __forceinline__ uint2 *row_segs(const Params &p, int64_t row) {
-    const size_t off = (kRowInfoBytes + 4 * static_cast<size_t>(p.plan.chunks_per_row) + 15) / 16 * 16;
-    return reinterpret_cast<uint2 *>(row_ws(p, row) + off);
+    return reinterpret_cast<uint2 *>(row_ws(p, row) + ws_seg_offset(p.plan.chunks_per_row));
 }
 
 __device__ __forceinline__ int64_t split_chunks(const Params &p, int64_t n) {
@@ -1052,7 +1122,11 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
 
     if (n > p.plan.direct_max) {
         // ---- split row: threshold guess from a strided sample (the whole
-        // row when it has at most kSampleSize columns)
+        // row when it has at most kSampleSize columns).  First clear the
+        // row's coarse candidate histogram, which the chunk kernel counts
+        // into once this grid has completed.
+        if (threadIdx.x < kCoarseBins / 4)
+            reinterpret_cast<uint4 *>(row_hist(p, row))[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
         int m;
         uint32_t kmin = 0xFFFFFFFFu, kmax = 0;
         // hint anchor (the previous argmax column): thread 32 issues its two
@@ -1122,6 +1196,7 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
             uint32_t *info = row_info(p, row);
             info[0] = t_lo;
             info[1] = static_cast<uint32_t>(bin_shift);
+            info[2] = 0;  // the row's chunk ticket (fused plans)
         }
         GBTOPK_TRACE_POINT(6, 0);
         GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | 3u);
@@ -1496,28 +1571,160 @@ struct SegMap {  // candidate j of the concatenated segments -> its address
 
 constexpr uint32_t kPadColumn = 0xFFFFFFFFu;  // marks a gather padding slot
 
+// Coarse bin holding the r-th largest of the candidates counted in
+// hist[kCoarseBins] (shared memory), found by warp 0 alone: c.bcast[2] =
+// the bin, c.bcast[3] = the count above it, c.bcast[4] = its count.
+// Requires 1 <= r <= the total count.  The caller syncs the block after it.
+__device__ __forceinline__ void coarse_select(const uint32_t *hist, uint32_t r, Ctrl &c,
+                                              uint32_t *fill = nullptr) {
+    static_assert(kCoarseBins == 256, "eight bins per lane");
+    if (threadIdx.x >= 32) return;
+    const uint32_t lane = lane_id();
+    uint32_t cnts[8], s = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {  // bins 255 - 8 lane - j, from the top
+        cnts[j] = hist[255 - 8 * lane - j];
+        s += cnts[j];
+    }
+    uint32_t incl = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= static_cast<uint32_t>(off)) incl += y;
+    }
+    const uint32_t excl = incl - s;
+    if (fill) {  // fill[b] = the count of the bins above b
+        uint32_t acc = excl;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            fill[255 - 8 * lane - j] = acc;
+            acc += cnts[j];
+        }
+    }
+    const uint32_t bal = __ballot_sync(0xffffffffu, excl < r && r <= incl);
+    if (bal != 0u && static_cast<int>(lane) == __ffs(bal) - 1) {
+        uint32_t acc = excl;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (acc + cnts[j] >= r) {
+                c.bcast[2] = 255u - 8u * lane - static_cast<uint32_t>(j);
+                c.bcast[3] = acc;
+                c.bcast[4] = cnts[j];
+                break;
+            }
+            acc += cnts[j];
+        }
+    }
+}
+
+// Index of this thread among the threads of the block with `flag` set (in
+// thread order), and their count.  All threads; uses c.scan; ends with a
+// barrier (c.scan free again).
+__device__ __forceinline__ uint32_t block_flag_index(bool flag, Ctrl &c, uint32_t &count) {
+    const uint32_t warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const uint32_t m = __ballot_sync(0xffffffffu, flag);
+    if (lane_id() == 0) c.scan[warp] = __popc(m);
+    __syncthreads();
+    uint32_t before = 0, tot = 0;
+    for (uint32_t w = 0; w < nw; ++w) {
+        const uint32_t v = c.scan[w];
+        before += w < warp ? v : 0u;
+        tot += v;
+    }
+    count = tot;
+    const uint32_t idx = before + __popc(m & lanemask_lt());
+    __syncthreads();
+    return idx;
+}
+
+// Radix select among one value per thread (`live` threads): the r-th
+// largest of the live values v (1 <= r <= live count), digit by digit over
+// 8-bit digits from the highest bit at which the live values differ (one
+// block AND/OR reduction finds it; equal values need no round).  Returns the
+// value and, in gt, how many live values exceed it.  All threads; uses
+// c.rhist, c.key_min, c.key_max.
+__device__ __forceinline__ uint32_t block_select_one(bool live, uint32_t v, uint32_t r, Ctrl &c, uint32_t &gt) {
+    if (threadIdx.x == 0) {
+        c.key_min = 0xFFFFFFFFu;  // AND of the live values
+        c.key_max = 0;            // OR of the live values
+    }
+    __syncthreads();
+    const uint32_t a = __reduce_and_sync(0xffffffffu, live ? v : 0xFFFFFFFFu);
+    const uint32_t o = __reduce_or_sync(0xffffffffu, live ? v : 0u);
+    if (lane_id() == 0) {
+        atomicAnd(&c.key_min, a);
+        atomicOr(&c.key_max, o);
+    }
+    __syncthreads();
+    const uint32_t kand = c.key_min, diff = kand ^ c.key_max;
+    if (diff == 0u) {  // every live value is the same
+        gt = 0;
+        return kand;
+    }
+    const int hb = 31 - __clz(diff);           // highest differing bit
+    uint32_t pmask = hb == 31 ? 0u : ~((2u << hb) - 1u);
+    uint32_t prefix = kand & pmask, rem = r;
+    for (int top = hb + 1; top > 0; top -= 8) {  // digits [top - 8, top), the last one clipped at bit 0
+        const int shift = top > 8 ? top - 8 : 0;
+        if (threadIdx.x < 256) c.rhist[threadIdx.x] = 0;
+        __syncthreads();
+        if (live && (v & pmask) == prefix) atomicAdd(&c.rhist[(v >> shift) & 255u], 1u);
+        __syncthreads();
+        coarse_select(c.rhist, rem, c);
+        __syncthreads();
+        const uint32_t dmask = (top >= 32 ? 0xFFFFFFFFu : ((1u << top) - 1u)) & ~((1u << shift) - 1u);
+        prefix |= (c.bcast[2] << shift) & dmask;
+        pmask |= dmask;
+        rem -= c.bcast[3];
+        __syncthreads();
+    }
+    gt = r - rem;
+    return prefix;
+}
+
+// The best `need` of the bsize (<= NT) members of blist, by key descending
+// and then by the tie mode's column order (any order for tie mode 0), into
+// sel[above, above + need) in no particular order: one member per thread,
+// the need-th key by block_select_one, then among the members equal to it
+// either the first in list order (tie mode 0) or the ones whose tie_key is
+// at most the (need - gt)-th smallest (a second select over the columns).
+template <int NT, class KeyOf>
+__device__ void select_members(const uint2 *blist, uint32_t bsize, uint32_t need, uint32_t above, int tie,
+                               uint2 *sel, Ctrl &c, KeyOf key_of) {
+    const uint32_t tid = threadIdx.x;
+    const bool live = tid < bsize;
+    const uint2 me = live ? blist[tid] : make_uint2(0u, 0u);
+    const uint32_t mk = live ? key_of(me.x) : 0u;
+    uint32_t gt;
+    const uint32_t t = block_select_one(live, mk, need, c, gt);
+    const uint32_t need_ties = need - gt;
+    const bool eq = live && mk == t;
+    bool take_eq;
+    if (tie == 0) {  // (tie is block-uniform; every thread takes part in the index)
+        uint32_t neq;
+        const uint32_t ei = block_flag_index(eq, c, neq);
+        take_eq = eq && ei < need_ties;
+    } else {
+        // the (need_ties)-th largest complement of tie_key = the columns to keep
+        uint32_t g2;
+        const uint32_t cm = ~tie_key(me.y, tie);
+        const uint32_t ct = block_select_one(eq, cm, need_ties, c, g2);
+        take_eq = eq && cm >= ct;
+    }
+    const bool take = (live && mk > t) || take_eq;
+    uint32_t ntake;
+    const uint32_t slot = block_flag_index(take, c, ntake);
+    if (take) sel[above + slot] = me;
+    __syncthreads();
+}
+
 // Completes sel[above, above + need) with the best `need` of the bsize
 // members of the boundary bin (blist), ranked by (key desc, column asc).
 template <int DT, int NT>
 __device__ bool rank_boundary(const uint2 *blist, uint32_t bsize, uint32_t need, uint32_t above, int tie,
                               uint2 *sel, Ctrl &c) {
-    const uint32_t tid = threadIdx.x;
-    if (bsize <= kRankMax) {
-        // one warp per member of bin b*: its rank among the others, counted across the lanes
-        const uint32_t w = tid >> 5, lane = lane_id();
-        for (uint32_t i = w; i < bsize; i += NT / 32) {
-            const uint2 me = blist[i];
-            const uint32_t mk = Elem<DT>::key(me.x);
-            uint32_t rank = 0;
-            for (uint32_t j2 = lane; j2 < bsize; j2 += 32) {
-                const uint2 o = blist[j2];
-                const uint32_t ok = Elem<DT>::key(o.x);
-                rank += (ok > mk || (ok == mk && tie_key(o.y, tie) < tie_key(me.y, tie))) ? 1u : 0u;
-            }
-            rank = __reduce_add_sync(0xffffffffu, rank);
-            if (lane == 0 && rank < need) sel[above + rank] = me;
-        }
-        __syncthreads();
+    if (bsize <= static_cast<uint32_t>(NT)) {
+        select_members<NT>(blist, bsize, need, above, tie, sel, c, [](uint32_t raw) { return Elem<DT>::key(raw); });
     } else {
         constexpr int KB = Elem<DT>::kKeyBits;
         const PairSrc<DT> bs{blist};
@@ -1535,178 +1742,94 @@ __device__ bool rank_boundary(const uint2 *blist, uint32_t bsize, uint32_t need,
     return true;
 }
 
-// Exact top-k among candidates gathered in shared memory: cand[0, total_p)
-// holds (raw, column) pairs, padding slots carry column kPadColumn, every
-// live candidate has key >= t_lo and at least k are live.  The keys are
-// histogrammed over kBins bins (bin_of), the bin b* holding the k-th key
-// from the top is found, the candidates of higher bins go to sel and b*'s
-// members to blist, ranked by (key desc, column asc) so the best `need`
-// complete sel[0, k).  `sel` may alias `hist`, whose kBins counters the
-// caller has zeroed.  All NT threads of the block call it; returns false
-// (nothing written) when b* holds more than kFinalBCap members.
-template <int DT, int NT>
-__device__ bool select_gathered(const uint2 *cand, uint32_t total_p, uint32_t t_lo, int bin_shift, int k,
-                                int tie, uint32_t *hist, uint2 *sel, uint2 *blist, Ctrl &c) {
-    const uint32_t tid = threadIdx.x;
-#pragma unroll 4
-    for (uint32_t i = tid; i < total_p; i += NT) {
-        const uint2 v = cand[i];
-        if (v.y != kPadColumn) atomicAdd(&hist[bin_of(Elem<DT>::key(v.x), t_lo, bin_shift)], 1u);
-    }
-    __syncthreads();
-    find_bin_from_top<NT>(hist, static_cast<uint32_t>(k), c);
-    const uint32_t bstar = c.bcast[2], above = c.bcast[3], bsize = c.bcast[4];
-    if (bsize > static_cast<uint32_t>(kFinalBCap)) return false;
-    // bins above b* go to sel, bin b* to blist (sel aliases the consumed
-    // histogram): each thread counts its candidates (every NT-th, so a
-    // warp's loads are consecutive), one block scan gives its output slots
-    uint32_t nhi = 0, neq = 0;
-    for (uint32_t i = tid; i < total_p; i += NT) {
-        const uint2 v = cand[i];
-        const uint32_t b = bin_of(Elem<DT>::key(v.x), t_lo, bin_shift);
-        const bool live = v.y != kPadColumn;
-        nhi += (live && b > bstar) ? 1u : 0u;
-        neq += (live && b == bstar) ? 1u : 0u;
-    }
-    uint32_t ptot;
-    const uint32_t pre = block_excl_scan((nhi << 16) | neq, c, ptot);
-    uint32_t hs = pre >> 16, es = pre & 0xFFFFu;
-    for (uint32_t i = tid; i < total_p && (nhi | neq); i += NT) {
-        const uint2 v = cand[i];
-        if (v.y == kPadColumn) continue;
-        const uint32_t b = bin_of(Elem<DT>::key(v.x), t_lo, bin_shift);
-        if (b > bstar) sel[hs++] = v;
-        else if (b == bstar) blist[es++] = v;
-    }
-    __syncthreads();
-    return rank_boundary<DT, NT>(blist, bsize, static_cast<uint32_t>(k) - above, above, tie, sel, c);
-}
+// Where a split row's finalize keeps its data in shared memory: the kBins
+// counters (the selection aliases them once they are consumed), the
+// boundary-bin list, one offset per chunk, the gathered candidates, and the
+// sorted-output scratch (which may reuse the list, offsets and candidates:
+// they are dead once the row is selected).
+struct FinalRegion {
+    uint32_t *fill;       // kCoarseBins slot counters of the classification pass
+    uint32_t *hist;
+    uint2 *sel;
+    uint2 *blist;
+    uint32_t bcap;        // boundary-bin members blist holds
+    uint32_t *choff;
+    uint2 *cand;
+    uint32_t gather_cap;  // candidates cand holds
+    uint8_t *scratch;     // det_scratch_bytes(sel_cap)
+};
 
-// Exact top-k among `total` (>= k) candidates left in workspace segments
-// (L2-resident; `map` numbers them consecutively), for rows whose
-// candidates do not fit in shared memory: two passes over the segments, the
-// first histogramming the keys, the second keeping the bins above the
-// boundary bin and collecting its members, which are ranked exactly.  Same
-// contract as select_gathered.
+// Exact top-k of split row `row` (n valid columns from col0, nch chunks)
+// from the candidates its chunks left in the workspace.  The k-th key is
+// located by a window search over the candidates' keys: first kCoarseBins
+// coarse bins above the guess t_lo (coarse_bin; the row's counters from the
+// workspace when the chunk kernel counted them (ws_hist), else one pass
+// over the candidates), then, while the window holding the k-th key has more
+// members than the boundary list holds, 8-bit sub-bins of that window.  One
+// counted pass then writes every candidate above the window (to its output
+// slot, or to the selection when the output is sorted) and lists the
+// window's members, which are ranked exactly.  The candidates are gathered
+// into shared memory by one bulk copy per chunk (each segment padded to an
+// even count so every copy starts on a 16-byte boundary; the padding slot is
+// marked with column kPadColumn), or read straight from L2 when they do not
+// fit.  Falls back to an exact radix select over the row in global memory
+// when a segment overflowed, the guess was too high (fewer than k
+// candidates) or more than the list holds share the k-th key.  `bar` is an
+// initialised barrier whose next phase has parity `parity`.  The next grid
+// on the stream is released (programmatic dependent launch) once the
+// selection is known.  All NT threads call it.
 template <int DT, int NT>
-__device__ bool select_from_segments(const SegMap &map, uint32_t total, uint32_t t_lo, int bin_shift, int k,
-                                     int tie, uint32_t *hist, uint2 *sel, uint2 *blist, Ctrl &c) {
-    constexpr int GB = 8;  // candidates in flight per thread
-    const uint32_t tid = threadIdx.x;
-#pragma unroll
-    for (int j = 0; j < kBins / NT; ++j) hist[tid + j * NT] = 0;
-    __syncthreads();
-    int cur = 0;
-    for (uint32_t b0 = 0; b0 < total; b0 += GB * NT) {
-        const uint2 *addr[GB];
-        uint32_t raw[GB];
-#pragma unroll
-        for (int u = 0; u < GB; ++u) {
-            const uint32_t j = b0 + u * NT + tid;
-            addr[u] = j < total ? map.at(j, cur) : nullptr;
-        }
-#pragma unroll
-        for (int u = 0; u < GB; ++u) raw[u] = addr[u] ? __ldcg(addr[u]).x : 0u;
-#pragma unroll
-        for (int u = 0; u < GB; ++u)
-            if (addr[u]) atomicAdd(&hist[bin_of(Elem<DT>::key(raw[u]), t_lo, bin_shift)], 1u);
-    }
-    __syncthreads();
-    find_bin_from_top<NT>(hist, static_cast<uint32_t>(k), c);
-    const uint32_t bstar = c.bcast[2], above = c.bcast[3], bsize = c.bcast[4];
-    if (bsize > static_cast<uint32_t>(kFinalBCap)) return false;
-    // bins above b* go to sel, bin b* to blist (count-then-write per batch)
-    uint32_t hi_base = 0, eq_base = 0;
-    int cur2 = 0;
-    for (uint32_t b0 = 0; b0 < total; b0 += GB * NT) {
-        const uint2 *addr[GB];
-        uint2 v[GB];
-        uint32_t hi_mask = 0, eq_mask = 0;
-#pragma unroll
-        for (int u = 0; u < GB; ++u) {
-            const uint32_t j = b0 + u * NT + tid;
-            addr[u] = j < total ? map.at(j, cur2) : nullptr;
-        }
-#pragma unroll
-        for (int u = 0; u < GB; ++u) v[u] = addr[u] ? __ldcg(addr[u]) : make_uint2(0, 0);
-#pragma unroll
-        for (int u = 0; u < GB; ++u) {
-            if (addr[u]) {
-                const uint32_t b = bin_of(Elem<DT>::key(v[u].x), t_lo, bin_shift);
-                hi_mask |= static_cast<uint32_t>(b > bstar) << u;
-                eq_mask |= static_cast<uint32_t>(b == bstar) << u;
-            }
-        }
-        const uint32_t packed = (static_cast<uint32_t>(__popc(hi_mask)) << 16) | __popc(eq_mask);
-        uint32_t ptot;
-        const uint32_t pre = block_excl_scan(packed, c, ptot);
-        uint32_t hs = hi_base + (pre >> 16), es = eq_base + (pre & 0xFFFFu);
-#pragma unroll
-        for (int u = 0; u < GB; ++u) {
-            if ((hi_mask >> u) & 1u) sel[hs++] = v[u];
-            if ((eq_mask >> u) & 1u) blist[es++] = v[u];
-        }
-        hi_base += ptot >> 16;
-        eq_base += ptot & 0xFFFFu;
-    }
-    __syncthreads();
-    return rank_boundary<DT, NT>(blist, bsize, static_cast<uint32_t>(k) - above, above, tie, sel, c);
-}
-
-template <int DT>
-__global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_constant__ Params p) {
+__device__ void finalize_row(const Params &p, int64_t row, int64_t n, int64_t col0, int64_t nch,
+                             const FinalRegion &fr, unsigned long long *bar, uint32_t parity, bool ws_hist,
+                             Ctrl &c, int64_t trace_idx) {
+    (void)trace_idx;  // the trace row of this block (GBTOPK_TRACE builds)
     using raw_t = typename Elem<DT>::raw_t;
-    extern __shared__ __align__(128) uint8_t smem[];
-    Ctrl &c = *reinterpret_cast<Ctrl *>(smem);
-    uint32_t *hist = reinterpret_cast<uint32_t *>(smem + kCtrlBytes);
-    uint2 *sel = reinterpret_cast<uint2 *>(smem + kCtrlBytes);  // aliases hist
-    uint2 *blist = reinterpret_cast<uint2 *>(smem + kCtrlBytes + p.plan.final_sel_bytes);
-    uint32_t *choff = reinterpret_cast<uint32_t *>(blist + kFinalBCap);
-    uint2 *cand = reinterpret_cast<uint2 *>(choff + kFinalThreads);  // gathered candidates
-    const uint32_t gather_cap = static_cast<uint32_t>(
-        (p.plan.final_smem - (kCtrlBytes + p.plan.final_sel_bytes + static_cast<size_t>(kFinalBCap) * 8 +
-                              4 * static_cast<size_t>(kFinalThreads))) / sizeof(uint2));
-    const int64_t row = p.row0 + blockIdx.x;
+    static_assert(NT >= kCoarseBins, "one coarse bin per thread");
     const int k = p.k;
     const bool sorted = sorted_output(p.deterministic);
     const int tie = tie_mode(p.deterministic);
     const int tid = threadIdx.x;
-    constexpr int kTraceBase = kTraceFinal;
-    (void)kTraceBase;
-    int64_t n, col0;
-    row_window(p, row, n, col0);
-    const int64_t nch = split_chunks(p, n);
-    if (nch == 0) return;
-    if (tid == 0) {
-        mbar_init(&c.bar);
-        c.bcast[5] = 0;
-    }
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    GBTOPK_TRACE_POINT(0, 0);
     const raw_t *xrow = static_cast<const raw_t *>(p.x) + row * p.row_stride + col0;
-    const uint32_t *info = row_info(p, row);
-    const uint32_t t_lo = __ldcg(info);
-    const int bin_shift = static_cast<int>(__ldcg(info + 1));
+    // the row's guess, chunk counts and coarse counters: independent L2 loads, all in flight at once
+    const uint2 info = __ldcg(reinterpret_cast<const uint2 *>(row_info(p, row)));
+    const uint32_t my = tid < nch ? __ldcg(row_counts(p, row) + tid) : 0u;
+    const uint32_t hcount = (ws_hist && tid < kCoarseBins) ? __ldcg(row_hist(p, row) + tid) : 0u;
+    const uint32_t t_lo = info.x;
+    const int bin_shift = static_cast<int>(info.y);
     const uint32_t cap = static_cast<uint32_t>(chunk_seg_cap(n, k, p.plan.chunk));
     const uint2 *segs = row_segs(p, row);
+    if (tid < kCoarseBins) c.rhist[tid] = hcount;
+    if (tid == 0) {
+        c.bcast[5] = 0;      // a chunk overflowed its segment
+        c.cand_count = 0;    // chunks with an odd count
+        c.sel_count = 0;
+        c.b_count = 0;
+    }
 
-    // chunk counts -> padded offsets (nch <= kFinalThreads, checked on the host)
-    const uint32_t my = tid < nch ? __ldcg(row_counts(p, row) + tid) : 0u;
+    // chunk counts -> padded offsets (nch <= NT, checked on the host)
     const bool over = my > cap;
     const uint32_t cnt = over ? 0u : my;
     const uint32_t padded = (cnt + 1u) & ~1u;
-    if (over) atomicOr(&c.bcast[5], 1u);
-    const int odd = __syncthreads_count(cnt & 1u);
+    __syncthreads();
+    {
+        const uint32_t ov = __ballot_sync(0xffffffffu, over), od = __ballot_sync(0xffffffffu, (cnt & 1u) != 0u);
+        if (lane_id() == 0) {
+            if (ov) atomicOr(&c.bcast[5], 1u);
+            if (od) atomicAdd(&c.cand_count, static_cast<uint32_t>(__popc(od)));
+        }
+    }
     uint32_t total_p;
-    const uint32_t poff = block_excl_scan(padded, c, total_p);
-    const uint32_t total = total_p - static_cast<uint32_t>(odd);
+    const uint32_t poff = block_excl_scan(padded, c, total_p);  // its barriers publish the flags
+    const uint32_t total = total_p - c.cand_count;
     bool fallback = c.bcast[5] != 0 || total < static_cast<uint32_t>(k);
-    const bool in_smem = total_p <= gather_cap;
+    const bool in_smem = total_p <= fr.gather_cap;
+    const bool gathered = !fallback && in_smem;  // block-uniform
     bool copy_ok = true;
-    if (!fallback && in_smem) {
+    if (tid == 0) GBTOPK_TRACE_SET(trace_idx, 8, -1);
+    if (gathered) {
         // ---- gather the segments into shared memory (one bulk copy per chunk)
         if (tid == 0) {
-            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&c.bar)),
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                          "r"(total_p * 8u)
                          : "memory");
         }
@@ -1714,47 +1837,377 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
         if (tid < nch && padded > 0) {
             asm volatile(
                 "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                    smem_u32(cand + poff)),
-                "l"(segs + static_cast<int64_t>(tid) * cap), "r"(padded * 8u), "r"(smem_u32(&c.bar))
+                    smem_u32(fr.cand + poff)),
+                "l"(segs + static_cast<int64_t>(tid) * cap), "r"(padded * 8u), "r"(smem_u32(bar))
                 : "memory");
         }
-        // zero the histogram while the copies land (it is not their destination)
-#pragma unroll
-        for (int j = 0; j < kBins / kFinalThreads; ++j) hist[tid + j * kFinalThreads] = 0;
-        copy_ok = wait_bar(p.ws, c, &c.bar, 0);
+        copy_ok = wait_bar(p.ws, c, bar, parity);
+        if (tid == 0) GBTOPK_TRACE_SET(trace_idx, 9, -1);
         if (copy_ok) {
-            if (tid < nch && (cnt & 1u)) cand[poff + cnt].y = kPadColumn;
+            if (tid < nch && (cnt & 1u)) fr.cand[poff + cnt].y = kPadColumn;
             __syncthreads();
-            GBTOPK_TRACE_POINT(1, 0);
-            if (!select_gathered<DT, kFinalThreads>(cand, total_p, t_lo, bin_shift, k, tie, hist, sel, blist, c))
-                fallback = true;
         } else {
             fallback = true;
         }
     } else if (!fallback) {
-        // ---- two passes straight over the segments in L2 (unpadded offsets)
-        const uint32_t base = block_excl_scan(cnt, c, total_p);
-        if (tid < nch) choff[tid] = base;
+        // ---- the L2 passes need unpadded offsets
+        uint32_t tot2;
+        const uint32_t base = block_excl_scan(cnt, c, tot2);
+        if (tid < nch) fr.choff[tid] = base;
         __syncthreads();
-        if (!select_from_segments<DT, kFinalThreads>(SegMap{segs, choff, static_cast<int>(nch), cap}, total, t_lo,
-                                                     bin_shift, k, tie, hist, sel, blist, c))
-            fallback = true;
     }
-    if (fallback) exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, tie, sel, c.rhist, c);
-    GBTOPK_TRACE_POINT(2, 0);
+    // visits every candidate once, in the same order on every call:
+    // f(live, pair); every thread makes the same number of calls
+    const SegMap map{segs, fr.choff, static_cast<int>(nch), cap};
+    auto for_each_cand = [&](auto &&f) {
+        if (in_smem) {
+            constexpr int GS = 4;  // independent candidates per thread per step (latency overlap)
+            for (uint32_t i0 = 0; i0 < total_p; i0 += GS * NT) {
+                uint2 v[GS];
+#pragma unroll
+                for (int u = 0; u < GS; ++u) {
+                    const uint32_t i = i0 + u * NT + tid;
+                    v[u] = i < total_p ? fr.cand[i] : make_uint2(0u, kPadColumn);
+                }
+#pragma unroll
+                for (int u = 0; u < GS; ++u) f(v[u].y != kPadColumn, v[u]);
+            }
+        } else {
+            constexpr int GB = 4;  // candidates in flight per thread
+            int cur = 0;
+            for (uint32_t j0 = 0; j0 < total; j0 += GB * NT) {
+                uint2 v[GB];
+#pragma unroll
+                for (int u = 0; u < GB; ++u) {
+                    const uint32_t j = j0 + u * NT + tid;
+                    v[u] = j < total ? __ldcg(map.at(j, cur)) : make_uint2(0u, kPadColumn);
+                }
+#pragma unroll
+                for (int u = 0; u < GB; ++u) f(j0 + u * NT + tid < total, v[u]);
+            }
+        }
+    };
+    uint32_t above = 0, bsize = 0;
+    if (!fallback) {
+        if (!ws_hist) {
+            for_each_cand([&](bool live, uint2 v) {
+                if (live) atomicAdd(&c.rhist[coarse_bin(Elem<DT>::key(v.x), t_lo, bin_shift)], 1u);
+            });
+            __syncthreads();
+        }
+        // ---- the window [w_lo, w_lo + 2^wbits) holding the k-th key, `above`
+        // candidates above it (wbits 32: open above); fr.fill[b] = the count
+        // of the coarse bins above b
+        coarse_select(c.rhist, static_cast<uint32_t>(k), c);
+        __syncthreads();
+        const int s0 = bin_shift + kCoarseShift;
+        uint32_t b = c.bcast[2];
+        above = c.bcast[3];
+        bsize = c.bcast[4];
+        uint32_t w_lo = t_lo + (b << s0);
+        int wbits = b == static_cast<uint32_t>(kCoarseBins - 1) ? 32 : s0;
+        while (bsize > fr.bcap && wbits > 0) {  // block-uniform: narrow the window by 8 bits
+            const int sub = wbits > 8 ? wbits - 8 : 0;
+            if (tid < kCoarseBins) c.rhist[tid] = 0;
+            __syncthreads();
+            const uint32_t wl = w_lo;
+            const uint64_t wspan = uint64_t{1} << wbits;
+            for_each_cand([&](bool live, uint2 v) {
+                const uint32_t key = Elem<DT>::key(v.x);
+                if (live && key >= wl && static_cast<uint64_t>(key - wl) < wspan)
+                    atomicAdd(&c.rhist[(key - wl) >> sub], 1u);
+            });
+            __syncthreads();
+            coarse_select(c.rhist, static_cast<uint32_t>(k) - above, c);
+            __syncthreads();
+            b = c.bcast[2];
+            above += c.bcast[3];
+            bsize = c.bcast[4];
+            w_lo += b << sub;
+            wbits = sub;
+        }
+        if (tid == 0) GBTOPK_TRACE_SET(trace_idx, 13, -1);
+        if (bsize > fr.bcap) fallback = true;  // block-uniform: more ties at the k-th key than the list holds
+        if (!fallback) {
+            // ---- candidates above the window to sel, its members to blist:
+            // count, one block scan, write (no per-candidate atomics)
+            const uint32_t wl = w_lo;
+            const uint64_t wspan = uint64_t{1} << wbits;
+            auto classify = [&](uint2 v, bool &hi, bool &eq) {
+                const uint32_t key = Elem<DT>::key(v.x);
+                const bool in = v.y != kPadColumn && key >= wl;
+                const bool up = static_cast<uint64_t>(key - wl) >= wspan;
+                hi = in && up;
+                eq = in && !up;
+            };
+            constexpr int RC = 32;  // candidates per thread whose marks fit in one word
+            if (in_smem && total_p <= static_cast<uint32_t>(RC * NT)) {
+                // the gathered candidates stay in shared memory: mark, then
+                // revisit only the marked ones
+                uint32_t hm = 0, em = 0;
+#pragma unroll 8
+                for (int u = 0; u < RC; ++u) {
+                    const uint32_t i = u * NT + tid;
+                    if (i < total_p) {
+                        bool hi, eq;
+                        classify(fr.cand[i], hi, eq);
+                        hm |= static_cast<uint32_t>(hi) << u;
+                        em |= static_cast<uint32_t>(eq) << u;
+                    }
+                }
+                uint32_t ptot;
+                const uint32_t pre = block_excl_scan((static_cast<uint32_t>(__popc(hm)) << 16) | __popc(em), c, ptot);
+                uint32_t hs = pre >> 16, es = pre & 0xFFFFu;
+                while (hm) {
+                    const int u = __ffs(hm) - 1;
+                    hm &= hm - 1;
+                    fr.sel[hs++] = fr.cand[u * NT + tid];
+                }
+                while (em) {
+                    const int u = __ffs(em) - 1;
+                    em &= em - 1;
+                    fr.blist[es++] = fr.cand[u * NT + tid];
+                }
+            } else {
+                uint32_t nhi = 0, neq = 0;
+                for_each_cand([&](bool live, uint2 v) {
+                    bool hi, eq;
+                    classify(v, hi, eq);
+                    nhi += (live && hi) ? 1u : 0u;
+                    neq += (live && eq) ? 1u : 0u;
+                });
+                uint32_t ptot;
+                const uint32_t pre = block_excl_scan((nhi << 16) | neq, c, ptot);
+                uint32_t hs = pre >> 16, es = pre & 0xFFFFu;
+                for_each_cand([&](bool live, uint2 v) {
+                    bool hi, eq;
+                    classify(v, hi, eq);
+                    if (live && hi) fr.sel[hs++] = v;
+                    if (live && eq) fr.blist[es++] = v;
+                });
+            }
+            __syncthreads();
+            if (tid == 0) GBTOPK_TRACE_SET(trace_idx, 14, -1);
+            if (tid == 0) GBTOPK_TRACE_SET(trace_idx, 5, static_cast<int64_t>(clock64()));
+            rank_boundary<DT, NT>(fr.blist, bsize, static_cast<uint32_t>(k) - above, above, tie, fr.sel, c);
+        }
+    }
+    // the exact select uses only the selection and the control block, never
+    // the gather region a timed-out copy may still be writing
+    if (fallback) exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, tie, fr.sel, c.rhist, c);
+    if (tid == 0) GBTOPK_TRACE_SET(trace_idx, 10, -1);
+    if (tid == 0) GBTOPK_TRACE_SET(trace_idx, 6, static_cast<int64_t>(clock64()));
+    if (tid == 0) GBTOPK_TRACE_SET(trace_idx, 11, (fallback ? 1 : 0) | (in_smem ? 2 : 0) | (static_cast<int64_t>(total) << 8));
     // the next call's first kernel may launch now (it waits for this grid
     // to complete before reading anything)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (!copy_ok && tid == 0) mbar_wait(&c.bar, 0);  // let the copies land (before reusing cand)
-    if (sorted) {
+    bool scratch_ok = true;
+    if (!copy_ok) {  // the sorted output's scratch overlaps the gather region
+        if (tid == 0) {
+            const bool landed = mbar_wait(bar, parity);
+            c.bcast[7] = landed ? 1u : 0u;
+            if (!landed) atomicOr(reinterpret_cast<uint32_t *>(p.ws), kStatusCopyLost);
+        }
         __syncthreads();
-        emit_sorted<DT, kFinalThreads>(p, row, sel, k, reinterpret_cast<uint8_t *>(cand), c);
-    } else {
-        emit<DT>(p, row, sel, k);
+        scratch_ok = c.bcast[7] != 0;
     }
+    if (sorted && scratch_ok) {
+        __syncthreads();
+        emit_sorted<DT, NT>(p, row, fr.sel, k, fr.scratch, c);
+    } else {
+        emit<DT>(p, row, fr.sel, k);  // the selected set, unordered if the scratch was unusable
+    }
+    if (tid == 0) GBTOPK_TRACE_SET(trace_idx, 12, -1);
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_constant__ Params p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    Ctrl &c = *reinterpret_cast<Ctrl *>(smem);
+    FinalRegion fr;
+    fr.hist = reinterpret_cast<uint32_t *>(smem + kCtrlBytes);
+    fr.sel = reinterpret_cast<uint2 *>(smem + kCtrlBytes);  // aliases hist
+    fr.blist = reinterpret_cast<uint2 *>(smem + kCtrlBytes + p.plan.final_sel_bytes);
+    fr.bcap = kFinalBCap;
+    fr.choff = reinterpret_cast<uint32_t *>(fr.blist + kFinalBCap);
+    fr.fill = fr.choff + kFinalThreads;
+    fr.cand = reinterpret_cast<uint2 *>(fr.fill + kCoarseBins);  // gathered candidates
+    fr.gather_cap = static_cast<uint32_t>(
+        (p.plan.final_smem - (kCtrlBytes + p.plan.final_sel_bytes + static_cast<size_t>(kFinalBCap) * 8 +
+                              4 * static_cast<size_t>(kFinalThreads) + 4 * static_cast<size_t>(kCoarseBins))) /
+        sizeof(uint2));
+    fr.scratch = reinterpret_cast<uint8_t *>(fr.cand);
+    const int64_t row = p.row0 + blockIdx.x;
+    constexpr int kTraceBase = kTraceFinal;
+    (void)kTraceBase;
+    int64_t n, col0;
+    row_window(p, row, n, col0);
+    const int64_t nch = split_chunks(p, n);
+    if (nch == 0) return;
+    if (threadIdx.x == 0) mbar_init(&c.bar);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    GBTOPK_TRACE_POINT(0, 0);
+    finalize_row<DT, kFinalThreads>(p, row, n, col0, nch, fr, &c.bar, 0, false, c, kTraceFinal + blockIdx.x);
     GBTOPK_TRACE_POINT(6, 0);
-    GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | (fallback ? 5u : (in_smem ? 4u : 3u)) |
-                              (static_cast<unsigned long long>(total) << 40));
+}
+
+// Chunk kernel (split rows of plans with top_k <= kPairSortMax): one block
+// per (row, chunk) slot of the launch, chunk j of a row covering its valid
+// columns [j * chunk, (j + 1) * chunk); slots past a row's chunk count exit
+// at once.  Each block stages its chunk by one bulk copy (issued before it
+// waits for the row kernel, whose blocks have all passed their own wait for
+// the stream's preceding grid, so the inputs are final), takes the row's
+// guess t_lo once the row kernel has completed, keeps the chunk's elements
+// >= t_lo (pass bits from one sweep over the stage, one block scan for the
+// output slots, values read back from the stage) in the chunk's segment of
+// the workspace and stores the chunk's count.  It then takes a ticket from
+// the row's counter (cleared by the row kernel): the block that completes
+// the row selects it exactly in its own shared memory (finalize_row), the
+// stage being free by then.  No block ever waits for another.
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 3) chunk_kernel(const __grid_constant__ Params p) {
+    using raw_t = typename Elem<DT>::raw_t;
+    constexpr int es = Elem<DT>::kBytes;
+    constexpr int EPV = 16 / es;
+    constexpr int VPT = kFusedStageBytes / 16 / kThreads + 1;  // stage vectors per thread
+    constexpr int NW = (VPT * EPV + 31) / 32;                   // pass-bit words per thread
+    static_assert(32 % EPV == 0, "a vector's pass bits never straddle two words");
+    static_assert(kThreads == kCoarseBins, "one coarse bin per thread");
+    static_assert(kBins * 4 + 12 * kPairSortMax <= kFusedOffSel, "sorted-output scratch below the selection");
+    extern __shared__ __align__(128) uint8_t smem[];
+    Ctrl &c = *reinterpret_cast<Ctrl *>(smem);
+    uint8_t *stage = smem + kCtrlBytes;
+    const int tid = threadIdx.x;
+    constexpr int kTraceBase = kTraceChunk;
+    (void)kTraceBase;
+    GBTOPK_TRACE_POINT(0, 0);
+    const int64_t cpr = p.plan.chunks_per_row;
+    const int64_t row = p.row0 + static_cast<int64_t>(blockIdx.x) / cpr;
+    const int64_t ch = static_cast<int64_t>(blockIdx.x) % cpr;
+    int64_t n, col0;
+    row_window(p, row, n, col0);
+    const int64_t nch = split_chunks(p, n);
+    if (ch >= nch) return;
+    const int64_t CH = p.plan.chunk;
+    const int64_t c0 = ch * CH;
+    const int len = static_cast<int>((n - c0) < CH ? (n - c0) : CH);
+    const raw_t *xrow = static_cast<const raw_t *>(p.x) + row * p.row_stride + col0;
+    const Span sp = span_of<DT>(xrow + c0, len);
+    if (tid == 0) {
+        mbar_init(&c.bar);
+        bulk_load(stage, sp.a0, sp.bytes, &c.bar);
+    }
+    // the row kernel's guess, cleared ticket and cleared histogram
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    GBTOPK_TRACE_POINT(1, 0);
+    uint32_t *info = row_info(p, row);
+    const uint2 guess = __ldcg(reinterpret_cast<const uint2 *>(info));  // t_lo, bin shift
+    if (tid == 0) c.sel_count = 0;
+    c.rhist[tid] = 0;  // the chunk's coarse candidate histogram (kThreads == kCoarseBins)
+    const bool ok = wait_bar(p.ws, c, &c.bar, 0);
+    GBTOPK_TRACE_POINT(2, 0);
+    if (ok) {
+        const int nvec = ((sp.off + len) * es + 15) >> 4;
+        const uint4 *svec = reinterpret_cast<const uint4 *>(stage);
+        const PassTest<DT> pass(guess.x);
+        uint32_t mw[NW];
+#pragma unroll
+        for (int w = 0; w < NW; ++w) mw[w] = 0;
+        uint32_t cnt = 0;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int v = tid + j * kThreads;
+            uint32_t b = 0;
+            if (v < nvec) {
+                b = pass.mask(svec[v]);
+                if (v == 0 || v >= nvec - 1) b &= valid_lanes<EPV>(v, nvec, sp.off, len);
+            }
+            mw[(j * EPV) / 32] |= b << ((j * EPV) % 32);
+            cnt += __popc(b);
+        }
+        // slots: one shared atomic per warp, lanes in order within the warp
+        const uint32_t lane = lane_id();
+        uint32_t incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= static_cast<uint32_t>(o)) incl += y;
+        }
+        const uint32_t wtotal = __shfl_sync(0xffffffffu, incl, 31);
+        uint32_t base = 0;
+        if (lane == 0 && wtotal != 0u) base = atomicAdd(&c.sel_count, wtotal);
+        // the warp's candidates in rounds: each lane with candidates left
+        // writes its next one, a round's slots consecutive across the lanes
+        // (coalesced stores)
+        uint32_t wslot = __shfl_sync(0xffffffffu, base, 0);
+        const uint32_t lt = lanemask_lt();
+        const uint32_t cap = static_cast<uint32_t>(chunk_seg_cap(n, p.k, p.plan.chunk));
+        uint2 *seg = row_segs(p, row) + ch * cap;
+        const int shift = static_cast<int>(guess.y);
+        const raw_t *selem = reinterpret_cast<const raw_t *>(stage);
+        const uint32_t colbase = static_cast<uint32_t>(c0 - sp.off);
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            uint32_t bits = mw[w];
+            while (__any_sync(0xffffffffu, bits != 0u)) {
+                const bool has = bits != 0u;
+                const uint32_t m = __ballot_sync(0xffffffffu, has);
+                if (has) {
+                    const int e = w * 32 + __ffs(bits) - 1;
+                    bits &= bits - 1;
+                    const int epos = (tid + (e / EPV) * kThreads) * EPV + (e % EPV);
+                    const uint32_t raw = static_cast<uint32_t>(selem[epos]);
+                    const uint32_t slot = wslot + __popc(m & lt);
+                    if (slot < cap) seg[slot] = make_uint2(raw, colbase + static_cast<uint32_t>(epos));
+                    atomicAdd(&c.rhist[coarse_bin(Elem<DT>::key(raw), guess.x, shift)], 1u);
+                }
+                wslot += __popc(m);
+            }
+        }
+    }
+    GBTOPK_TRACE_POINT(3, 0);
+    // the chunk's coarse histogram into the row's (one add per nonempty
+    // bin), then the ticket: the barriers and thread 0's fence order every
+    // candidate, count and add of the block before it
+    __syncthreads();
+    if (ok && c.rhist[tid] != 0u) atomicAdd(row_hist(p, row) + tid, c.rhist[tid]);
+    __syncthreads();
+    if (tid == 0) {
+        row_counts(p, row)[ch] = ok ? c.sel_count : 0xFFFFFFFFu;  // an unread chunk: the row falls back
+        __threadfence();
+        const uint32_t done = atomicAdd(info + 2, 1u);
+        const bool is_last = done == static_cast<uint32_t>(nch - 1);
+        if (is_last) __threadfence();  // acquire: every chunk's candidates, counts and histogram
+        c.bcast[6] = is_last ? 1u : 0u;
+    }
+    __syncthreads();
+    const bool last = c.bcast[6] != 0;
+    GBTOPK_TRACE_POINT(4, 0);
+    GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | (last ? 1u : 0u) |
+                              (static_cast<unsigned long long>(ch) << 40));
+    bool stage_ok = ok;
+    if (!ok) {  // the stage copy may still land: wait (bounded) before the stage is reused or left
+        if (tid == 0) {
+            const bool landed = mbar_wait(&c.bar, 0);
+            c.bcast[7] = landed ? 1u : 0u;
+            if (!landed) atomicOr(reinterpret_cast<uint32_t *>(p.ws), kStatusCopyLost);
+        }
+        __syncthreads();
+        stage_ok = c.bcast[7] != 0;
+    }
+    if (!last) return;
+    if (!stage_ok) return;  // the row's outputs stay unwritten; the status word says so
+    FinalRegion fr;
+    fr.hist = nullptr;
+    fr.sel = reinterpret_cast<uint2 *>(stage + kFusedOffSel);
+    fr.blist = reinterpret_cast<uint2 *>(stage);
+    fr.bcap = kFusedBCap;
+    fr.choff = reinterpret_cast<uint32_t *>(stage + kFusedOffChOff);
+    fr.fill = reinterpret_cast<uint32_t *>(stage + kFusedOffFill);
+    fr.cand = reinterpret_cast<uint2 *>(stage + kFusedOffCand);
+    fr.gather_cap = kFusedGatherCap;
+    fr.scratch = stage;  // det_scratch_bytes(2048) = 40 KB, below the selection
+    finalize_row<DT, kThreads>(p, row, n, col0, nch, fr, &c.bar, 1, true, c, kTraceChunk + blockIdx.x);
 }
 
 // ---------------------------------------------------------------- small rows
@@ -1892,22 +2345,33 @@ cudaError_t launch_small(const Params &p, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, small_kernel<DT, NE>, p);
 }
 
+// Opts kernel `kern` into `bytes` of dynamic shared memory on the current
+// device when that is above the 48 KB default.  The attribute is per device
+// and per kernel, so the largest opt-in so far is remembered per (device,
+// kernel), under a lock shared by every host thread.
+std::mutex g_smem_mutex;
+std::map<std::pair<int, const void *>, size_t> g_smem_opted;
+
 template <class K>
-cudaError_t set_smem(K kern, size_t bytes, size_t &configured) {
-    if (bytes > 48 * 1024 && bytes > configured) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
-        if (e != cudaSuccess) return e;
-        configured = bytes;
-    }
+cudaError_t set_smem(K kern, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const std::pair<int, const void *> key(dev, reinterpret_cast<const void *>(kern));
+    std::lock_guard<std::mutex> lock(g_smem_mutex);
+    const auto it = g_smem_opted.find(key);
+    if (it != g_smem_opted.end() && it->second >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e != cudaSuccess) return e;
+    g_smem_opted[key] = bytes;
     return cudaSuccess;
 }
 
 template <int DT, int VPT>
 cudaError_t launch_row(const Params &p, cudaStream_t stream) {
-    static size_t configured = 0;  // largest dynamic smem opted in so far
     const size_t bytes = sorted_output(p.deterministic) ? p.plan.row_smem_sorted : p.plan.row_smem;
-    const cudaError_t e = set_smem(row_kernel<DT, VPT>, bytes, configured);
+    const cudaError_t e = set_smem(row_kernel<DT, VPT>, bytes);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1934,7 +2398,6 @@ cudaError_t launch_row_any(const Params &p, cudaStream_t stream) {
 
 template <int DT>
 cudaError_t launch_dt(const Params &p0, cudaStream_t stream) {
-    static size_t cfg_stream = 0, cfg_final = 0;  // largest opt-in so far
     cudaError_t e;
     if (!p0.plan.split) {
         Params p = p0;
@@ -1947,8 +2410,31 @@ cudaError_t launch_dt(const Params &p0, cudaStream_t stream) {
         }
         return launch_row_any<DT>(p, stream);
     }
-    if ((e = set_smem(stream_kernel<DT>, p0.plan.stream_smem, cfg_stream)) != cudaSuccess) return e;
-    if ((e = set_smem(final_kernel<DT>, p0.plan.final_smem, cfg_final)) != cudaSuccess) return e;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    if (p0.plan.fused) {
+        // row kernel (guesses, short rows), then one chunk-kernel block per
+        // (row, chunk) slot, in launches of up to block_rows rows
+        if ((e = set_smem(chunk_kernel<DT>, p0.plan.fused_smem)) != cudaSuccess) return e;
+        for (int64_t r0 = 0; r0 < p0.num_rows; r0 += p0.plan.block_rows) {
+            Params p = p0;
+            p.row0 = r0;
+            p.rows = (p0.num_rows - r0) < p0.plan.block_rows ? (p0.num_rows - r0) : p0.plan.block_rows;
+            if ((e = launch_row_any<DT>(p, stream)) != cudaSuccess) return e;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(p.rows * p.plan.chunks_per_row));
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = p.plan.fused_smem;
+            cfg.stream = stream;
+            cfg.attrs = pdl;
+            cfg.numAttrs = 1;
+            if ((e = cudaLaunchKernelEx(&cfg, chunk_kernel<DT>, p)) != cudaSuccess) return e;
+        }
+        return cudaGetLastError();
+    }
+    if ((e = set_smem(stream_kernel<DT>, p0.plan.stream_smem)) != cudaSuccess) return e;
+    if ((e = set_smem(final_kernel<DT>, p0.plan.final_smem)) != cudaSuccess) return e;
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;

@@ -548,16 +548,16 @@ def test_more_rows_than_one_launch(dev):
 
 @pytest.mark.parametrize("k", [1, 2048])
 def test_widest_rows(dev, k):
-    """Rows of 4 M fp32 columns (512 chunks, the plan's limit): most of a row's
-    candidates overflow the shared gather buffer, so the finalize takes the
-    two-pass path over the segments in L2."""
+    """Rows of 4 M fp32 columns (the plan's width limit: 256 chunks of the
+    two-kernel path): most of a row's candidates overflow the shared gather
+    buffer, so the finalize takes the two-pass path over the segments in L2."""
     g = torch.Generator().manual_seed(8200 + k)
     W = 512 * 8192
     x = torch.randn(2, W, generator=g)
     x[1, ::1000] += 5.0                                  # a heavy tail in row 1
     c = workloads.VarlenCase("widest", x, torch.tensor([W, W - 12345], dtype=torch.int32), k)
     run_case(dev, c, poison=False)
-    assert gb.gbtopk_plan_query(2, W, k, torch.float32)["chunks_per_row"] == 512
+    assert gb.gbtopk_plan_query(2, W, k, torch.float32)["chunks_per_row"] == 256
 
 
 def test_wider_than_the_plan_is_refused(dev):
@@ -776,3 +776,122 @@ def test_page_table_cu_seqlens_tie_large(dev):
         assert int((o[r] == -1).sum()) == k - m, f"row {r}: -1 count"
         got = sorted(inv[int(v)] for v in o[r].tolist() if v != -1)
         assert got == sorted(ref[r][:m].tolist()), f"row {r}: selected set differs"
+
+
+# ------------------------------------------------------------------ window edges
+
+def _wild_windows(R, W, seed, dtype=torch.float32, stride=None):
+    """Page-table style rows whose windows reach every edge case of the window
+    reading: lengths past the width (clamped), starts below 0, at the width and
+    past it (empty rows), zero lengths, plus ordinary windows."""
+    g = torch.Generator().manual_seed(seed)
+    S = stride or W
+    storage = torch.full((R, S), 3.0e38)
+    storage[:, :W] = torch.randn(R, W, generator=g)
+    scores = storage[:, :W].to(dtype) if dtype != torch.float32 else storage[:, :W]
+    lengths = torch.randint(0, W + 300, (R,), generator=g, dtype=torch.int32)
+    starts = torch.randint(0, W + 1, (R,), generator=g, dtype=torch.int32)
+    kind = torch.randint(0, 10, (R,), generator=g)
+    for r in range(R):
+        if kind[r] == 0:
+            starts[r] = -int(torch.randint(1, 60, (1,), generator=g))
+        elif kind[r] == 1:
+            starts[r] = W + int(torch.randint(1, 60, (1,), generator=g))
+        elif kind[r] == 2:
+            starts[r] = W
+        elif kind[r] == 3:      # runs past the width by a random amount
+            starts[r] = int(torch.randint(0, W, (1,), generator=g))
+            lengths[r] = W - int(starts[r]) + int(torch.randint(1, 5000, (1,), generator=g))
+    return scores, lengths, starts
+
+
+def _window_lengths(lengths, starts, W):
+    return [oracle.ragged_length(int(lengths[r]), int(starts[r]), W) for r in range(len(lengths))]
+
+
+# small-warp rows (width <= 2048, unsorted), rows finished by the row kernel,
+# and split rows
+WINDOW_PATHS = [(96, 1500, 256), (48, 12000, 1024), (24, 70000, 2048)]
+
+
+@pytest.mark.parametrize("R,W,k", WINDOW_PATHS)
+@pytest.mark.parametrize("det", [False, True])
+def test_page_table_window_and_table_edges(dev, R, W, k, det):
+    """Compact page table, page_size 64, with wild windows and page-table row
+    starts that put translated columns before and past the table (-1 in out,
+    idx kept in out_raw)."""
+    scores, lengths, starts = _wild_windows(R, W, 9100 + W, stride=W + 24)
+    g = torch.Generator().manual_seed(9200 + W)
+    ps = 64
+    P = (W + ps - 1) // ps + 3
+    pt = torch.randint(0, 1_000_000, (R, P), generator=g, dtype=torch.int32)
+    prs = torch.randint(-4, P, (R,), generator=g, dtype=torch.int32)
+    raw = torch.empty(R, k, dtype=torch.int32, device=dev)
+    out, _ = gb.top_k_page_table_transform(
+        _to_dev_strided(scores, dev), lengths.to(dev), pt.to(dev), k, ps, starts.to(dev),
+        prs.to(dev), out_raw_indices=raw, deterministic=det)
+    torch.cuda.synchronize(dev)
+    ref_out, ref_raw = oracle.page_table_transform(scores, lengths, pt, k, ps, starts, prs)
+    n = _window_lengths(lengths, starts, W)
+    assert any(n[r] == 0 and int(lengths[r]) > 0 for r in range(R)), "no empty-start row drawn"
+    assert any(int(starts[r]) >= 0 and int(lengths[r]) > W - int(starts[r]) > 0
+               for r in range(R)), "no clamped row drawn"
+    assert bool((ref_out == -1).logical_and(ref_raw >= 0).any()), "no out-of-table column drawn"
+    if det:
+        assert torch.equal(raw.cpu(), ref_raw)
+        assert torch.equal(out.cpu(), ref_out)
+        return
+    check_rows(scores, n, k, raw, ref_raw, None, col0=[max(0, int(s)) for s in starts])
+    o, rr = out.cpu(), raw.cpu()
+    for r in range(R):          # out is the translation of out_raw, slot by slot
+        for j in range(k):
+            idx = int(rr[r, j])
+            if idx < 0:
+                assert int(o[r, j]) == -1
+                continue
+            col = int(prs[r]) + idx // ps
+            want = -1 if (col < 0 or col >= P) else int(pt[r, col]) * ps + idx % ps
+            assert int(o[r, j]) == want, (r, j, idx)
+
+
+@pytest.mark.parametrize("R,W,k", WINDOW_PATHS)
+@pytest.mark.parametrize("det", [False, True])
+def test_ragged_transform_window_edges(dev, R, W, k, det):
+    """Ragged KV offset transform with wild windows."""
+    scores, lengths, starts = _wild_windows(R, W, 9300 + W)
+    g = torch.Generator().manual_seed(9400 + W)
+    offsets = torch.randint(-1000, 10_000_000, (R,), generator=g, dtype=torch.int32)
+    out = gb.top_k_ragged_transform(scores.to(dev), lengths.to(dev), offsets.to(dev), k,
+                                    row_starts=starts.to(dev), deterministic=det)
+    torch.cuda.synchronize(dev)
+    ref = oracle.ragged_offset_transform(scores, lengths, offsets, k, starts)
+    if det:
+        assert torch.equal(out.cpu(), ref)
+        return
+    raw = out.cpu().clone()
+    live = raw >= 0
+    raw[live] -= offsets.view(-1, 1).expand_as(raw)[live]
+    refraw = ref.clone()
+    refraw[ref >= 0] -= offsets.view(-1, 1).expand_as(ref)[ref >= 0]
+    check_rows(scores, _window_lengths(lengths, starts, W), k, raw, refraw, None,
+               col0=[max(0, int(s)) for s in starts])
+
+
+@pytest.mark.parametrize("R,W,k", WINDOW_PATHS)
+def test_page_table_cu_seqlens_window_edges(dev, R, W, k):
+    """Per-request page table (page_size 1) with wild windows, a table
+    narrower than the width (indices past it give -1) and uncovered rows;
+    deterministic, so the output must equal the oracle's bit for bit."""
+    scores, lengths, starts = _wild_windows(R, W, 9500 + W)
+    g = torch.Generator().manual_seed(9600 + W)
+    cuts = sorted(torch.randint(0, R - 2, (5,), generator=g).tolist())
+    cu = torch.tensor([0] + cuts + [R - 2], dtype=torch.int32)   # the last two rows: no request
+    B = cu.numel() - 1
+    P = W - W // 5
+    pt = torch.randint(0, 2_000_000_000, (B, P), generator=g, dtype=torch.int32)
+    out = gb.top_k_page_table_transform_cu_seqlens(
+        scores.to(dev), lengths.to(dev), pt.to(dev), cu.to(dev), k, row_starts=starts.to(dev),
+        deterministic=True)
+    torch.cuda.synchronize(dev)
+    ref = oracle.seqs_page_table_transform(scores, lengths, pt, cu, k, starts)
+    assert torch.equal(out.cpu(), ref)

@@ -6,8 +6,9 @@ allocations, inside plugin hosts), the library offers a variant that uses a
 16 MiB scratch buffer compiled into the library instead of a caller
 workspace.  These tests call it through the C ABI and check that, on two
 calls in a row sharing that buffer, it returns what gbtopk_varlen returns
-with a caller-owned workspace: bit-identical in deterministic mode, the same
-tie-aware selection otherwise.  This file is collected last on purpose.
+with a caller-owned workspace (bit-identical in deterministic mode, the same
+tie-aware selection otherwise) and that both agree with the CPU oracle.
+This file is collected last on purpose.
 """
 import pytest
 import torch
@@ -55,8 +56,11 @@ def test_static_scratch_matches_caller_workspace(dev, case):
     seq = c.seq_lens.to(dev)
     hint = c.pre_idx.to(dev) if c.pre_idx is not None else None
     n = oracle.row_lengths(c.seq_lens.tolist(), R, c.next_n, c.compress_ratio, W)
+    orc_i, _ = oracle.topk_varlen(c.logits, c.seq_lens, c.top_k, c.next_n, c.compress_ratio,
+                                  return_values=False)
     for det in (True, False):
         ref_i, ref_v = _reference(c, dev, det)
+        check_rows(c.logits, n, c.top_k, ref_i, orc_i, ref_v, deterministic=det)
         for call in range(2):   # two calls in a row share the library's scratch
             out = torch.full((R, c.top_k), 7, dtype=torch.int32, device=dev)
             val = torch.zeros((R, c.top_k), dtype=c.logits.dtype, device=dev)
@@ -72,6 +76,7 @@ def test_static_scratch_matches_caller_workspace(dev, case):
                                               else torch.int32))
             else:
                 check_rows(c.logits, n, c.top_k, out, ref_i, val)
+            check_rows(c.logits, n, c.top_k, out, orc_i, val, deterministic=det)
 
 
 def test_static_scratch_refuses_oversized_geometry(dev):
