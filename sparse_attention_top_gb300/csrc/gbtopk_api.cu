@@ -1,6 +1,7 @@
 // Host side of gbtopk: argument checks, the launch plan, and the C ABI
 // declared in include/gbtopk.h.  No device data is ever read on the host.
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 
 #include <cuda_runtime.h>
@@ -167,7 +168,26 @@ int check_common(const void *x, int dtype, int64_t num_rows, int64_t width, int6
     return GBTOPK_OK;
 }
 
-int launch(int dtype, const Params &p, void *stream) {
+// Poll limit of the first bounded wait on each bulk copy: kSpinLimit, or
+// the positive value of the environment variable GBTOPK_WAIT_POLLS (read
+// once per process).  A small value makes those waits give up, which runs
+// the recovery path (the affected rows are recomputed from global memory,
+// the status word's timeout bit is set) without any fault.
+uint32_t first_wait_polls() {
+    static const uint32_t polls = [] {
+        const char *v = std::getenv("GBTOPK_WAIT_POLLS");
+        if (!v || !*v) return gbtopk::kSpinLimit;
+        char *end = nullptr;
+        const unsigned long x = std::strtoul(v, &end, 10);
+        return (end && *end == '\0' && x > 0 && x <= gbtopk::kSpinLimit) ? static_cast<uint32_t>(x)
+                                                                         : gbtopk::kSpinLimit;
+    }();
+    return polls;
+}
+
+int launch(int dtype, const Params &p0, void *stream) {
+    Params p = p0;
+    p.wait_polls = first_wait_polls();
     const cudaError_t e = gbtopk::launch_topk(dtype, p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GBTOPK_OK : GBTOPK_ECUDA;
 }

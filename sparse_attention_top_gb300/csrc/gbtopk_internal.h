@@ -118,7 +118,8 @@ struct Params {
     const int32_t *idx_offset;    // ragged KV: out = idx + idx_offset[row] (null: none)
     const int32_t *cu_seqlens_q;  // page-table row = request of the score row (null: the row itself)
     int64_t num_reqs;
-    uint8_t *ws;   // status word at ws[0]; per-row blocks from kWsHeaderBytes
+    uint8_t *ws;   // status word at ws[0], the call's stream abort word at ws[4]; per-row blocks from kWsHeaderBytes
+    uint32_t wait_polls;  // poll limit of each first bounded wait on a bulk copy (kSpinLimit unless testing)
     int64_t row0;  // first row of this launch (the split pipeline runs in row blocks)
     int64_t rows;  // rows of this launch
     Plan plan;

@@ -129,7 +129,8 @@ struct Ctrl {
     uint32_t cand_count;
     uint32_t b_count;
     uint32_t key_max;
-    uint32_t pad[3];
+    uint32_t abort_flag;     // stream kernel: a bounded wait gave up, stop streaming
+    uint32_t pad[2];
     uint32_t scan[72];
     uint32_t rhist[256];     // radix-select digit histogram
     uint32_t key_min;
@@ -276,18 +277,32 @@ __device__ __forceinline__ void bulk_load(void *dst_smem, const void *src_gmem, 
         : "memory");
 }
 
-// Waits for phase `parity` of the barrier; gives up after kSpinLimit polls.
-__device__ __forceinline__ bool mbar_wait(unsigned long long *bar, uint32_t parity) {
-    for (uint32_t it = 0; it < kSpinLimit; ++it) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-            : "=r"(done)
-            : "r"(smem_u32(bar)), "r"(parity)
-            : "memory");
-        if (done) return true;
-    }
+__device__ __forceinline__ bool mbar_try(unsigned long long *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Waits for phase `parity` of the barrier; gives up after `limit` polls.
+__device__ __forceinline__ bool mbar_wait(unsigned long long *bar, uint32_t parity, uint32_t limit = kSpinLimit) {
+    for (uint32_t it = 0; it < limit; ++it)
+        if (mbar_try(bar, parity)) return true;
     return false;
+}
+
+// mbar_wait that also gives up when *abort becomes nonzero (checked every
+// 64 polls): 1 when the phase completed, 0 on the poll limit, 2 on abort.
+__device__ __forceinline__ int mbar_wait_or_abort(unsigned long long *bar, uint32_t parity, uint32_t limit,
+                                                  const volatile uint32_t *abort) {
+    for (uint32_t it = 0; it < limit; ++it) {
+        if (mbar_try(bar, parity)) return 1;
+        if ((it & 63u) == 63u && *abort) return 2;
+    }
+    return 0;
 }
 
 template <typename R>
@@ -721,9 +736,9 @@ __device__ __forceinline__ Span span_of(const typename Elem<DT>::raw_t *src, int
 // Block-uniform bounded wait on a stage barrier.  On timeout the status
 // word is flagged and false is returned (the caller recomputes from global
 // memory).
-__device__ bool wait_bar(uint8_t *ws, Ctrl &c, unsigned long long *bar, uint32_t parity) {
+__device__ bool wait_bar(uint8_t *ws, Ctrl &c, unsigned long long *bar, uint32_t parity, uint32_t limit) {
     if (threadIdx.x == 0) {
-        const bool ok = mbar_wait(bar, parity);
+        const bool ok = mbar_wait(bar, parity, limit);
         c.bcast[7] = ok ? 1u : 0u;
         if (!ok) atomicOr(reinterpret_cast<uint32_t *>(ws), kStatusWaitTimeout);
     }
@@ -1118,6 +1133,9 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
     if (threadIdx.x == 0) {
         c.key_min = 0xFFFFFFFFu;
         c.key_max = 0;
+        // this call's stream abort word, read by the finalize kernel once
+        // the stream kernel has completed
+        if (p.plan.split && blockIdx.x == 0) reinterpret_cast<uint32_t *>(p.ws)[1] = 0;
     }
 
     if (n > p.plan.direct_max) {
@@ -1232,7 +1250,7 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
     __syncthreads();
     const Span sp = span_of<DT>(xrow, n);
     if (threadIdx.x == 0) bulk_load(stage, sp.a0, sp.bytes, &c.bar);
-    const bool ok = wait_bar(p.ws, c, &c.bar, 0);
+    const bool ok = wait_bar(p.ws, c, &c.bar, 0, p.wait_polls);
     __syncthreads();
     GBTOPK_TRACE_POINT(3, 0);
     const raw_t *srow = reinterpret_cast<const raw_t *>(stage) + sp.off;
@@ -1267,12 +1285,21 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
                                                         k, tie, sel, lcand + total, stage_pairs - total, c);
     }
     if (!done) exact_select<DT>(GlobalSrc<DT>{xrow}, n, k, tie, sel, c.rhist, c);
-    if (!ok && threadIdx.x == 0) mbar_wait(&c.bar, 0);  // let the copy land before reusing the stage
-    if (sorted) {
+    bool stage_ok = ok;
+    if (!ok) {  // let the copy land before the stage is reused (bounded)
+        if (threadIdx.x == 0) {
+            const bool landed = mbar_wait(&c.bar, 0);
+            c.bcast[7] = landed ? 1u : 0u;
+            if (!landed) atomicOr(reinterpret_cast<uint32_t *>(p.ws), kStatusCopyLost);
+        }
+        __syncthreads();
+        stage_ok = c.bcast[7] != 0;
+    }
+    if (sorted && stage_ok) {
         __syncthreads();
         emit_sorted<DT, kThreads>(p, row, sel, k, stage, c);  // the stage is free once the row is selected
     } else {
-        emit<DT>(p, row, sel, k);
+        emit<DT>(p, row, sel, k);  // the selected set, unordered if the stage was unusable
     }
     GBTOPK_TRACE_POINT(6, 0);
     GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | 2u);
@@ -1363,6 +1390,7 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
     }
     if (threadIdx.x == 0) {
         rf[rows].prefix = total_items;
+        c.abort_flag = 0;
         for (int s = 0; s < kStages; ++s) {
             mbar_init_count(&c.full[s], 1);
             mbar_init_count(&c.empty[s], kGroupWarps);
@@ -1381,6 +1409,8 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
 #ifdef GBTOPK_TRACE
             unsigned long long p_wait = 0;
 #endif
+            int64_t issued = 0;
+            bool aborted = false;
             for (int64_t i = 0;; ++i) {
                 const int64_t item = blockIdx.x + i * G;
                 if (item >= total_items) break;
@@ -1389,13 +1419,15 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
                     const uint32_t par = static_cast<uint32_t>(((i / kStages) - 1) & 1);
 #ifdef GBTOPK_TRACE
                     const unsigned long long pa = clock64();
-                    const bool got = mbar_wait(&c.empty[s], par);
-                    p_wait += clock64() - pa;
-                    if (!got) {
-#else
-                    if (!mbar_wait(&c.empty[s], par)) {
 #endif
+                    const int got = mbar_wait_or_abort(&c.empty[s], par, p.wait_polls, &c.abort_flag);
+#ifdef GBTOPK_TRACE
+                    p_wait += clock64() - pa;
+#endif
+                    if (got != 1) {  // stop streaming: the consumers stop too
+                        atomicExch(&c.abort_flag, 1u);
                         atomicOr(reinterpret_cast<uint32_t *>(p.ws), kStatusWaitTimeout);
+                        aborted = true;
                         break;
                     }
                 }
@@ -1420,131 +1452,149 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
                 m.chunk = static_cast<int32_t>(chunk);
                 m.seg_cap = chunk_seg_cap(f.n, p.k, p.plan.chunk);
                 bulk_load(stages + static_cast<size_t>(s) * kStageBytes, sp.a0, sp.bytes, &c.full[s]);
+                issued = i + 1;
             }
 #ifdef GBTOPK_TRACE
             if (kTraceBase + blockIdx.x < kTraceBlocks) g_trace[kTraceBase + blockIdx.x][12] = p_wait;
 #endif
+            c.bcast[0] = static_cast<uint32_t>(issued);  // for the drain below
+            (void)aborted;
         }
         asm volatile("griddepcontrol.wait;" ::: "memory");
-        GBTOPK_TRACE_POINT(6, 0);
-        return;
-    }
+    } else {
+        // ---- consumers: the row kernel's guesses (programmatic dependent launch)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        for (int r = threadIdx.x - 32; r < rows; r += NCW * 32)
+            if (rf[r].n > p.plan.direct_max) rf[r].t_lo = __ldcg(row_info(p, p.row0 + r));
+        asm volatile("bar.sync 1, %0;" ::"r"(NCW * 32) : "memory");
 
-    // ---- consumers: the row kernel's guesses (programmatic dependent launch)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (int r = threadIdx.x - 32; r < rows; r += NCW * 32)
-        if (rf[r].n > p.plan.direct_max) rf[r].t_lo = __ldcg(row_info(p, p.row0 + r));
-    asm volatile("bar.sync 1, %0;" ::"r"(NCW * 32) : "memory");
-
-    const int cw = warp - 1;
-    const int grp = cw / kGroupWarps, gw = cw % kGroupWarps;
-    const int my_items = blockIdx.x < total_items
-                             ? static_cast<int>((total_items - blockIdx.x + G - 1) / G) : 0;
-#ifdef GBTOPK_TRACE
-    unsigned long long t_wait = 0, t_busy = 0, t_mark = clock64(), n_items = 0;
-#endif
-    for (int i = grp; i < my_items; i += kGroups) {
-        const int s = i % kStages;
-        const uint32_t par = static_cast<uint32_t>((i / kStages) & 1);
-#ifdef GBTOPK_TRACE
-        unsigned long long t_a = clock64();
-        t_busy += t_a - t_mark;
-#endif
-        const bool ok = mbar_wait(&c.full[s], par);
-#ifdef GBTOPK_TRACE
-        t_mark = clock64();
-        t_wait += t_mark - t_a;
-        ++n_items;
-#endif
-        const StageMeta m = meta[s];
-        const int64_t grow = p.row0 + m.row;
-        const int nvec = ((m.off + m.len) * es + 15) >> 4;
-        const uint4 *svec = reinterpret_cast<const uint4 *>(stages + static_cast<size_t>(s) * kStageBytes);
-        const int vbase = gw * 32 + static_cast<int>(lane);
-        uint4 w[VPL];
-        if (ok) {
-#pragma unroll
+        const int cw = warp - 1;
+        const int grp = cw / kGroupWarps, gw = cw % kGroupWarps;
+        const int my_items = blockIdx.x < total_items
+                                 ? static_cast<int>((total_items - blockIdx.x + G - 1) / G) : 0;
+    #ifdef GBTOPK_TRACE
+        unsigned long long t_wait = 0, t_busy = 0, t_mark = clock64(), n_items = 0;
+    #endif
+        for (int i = grp; i < my_items; i += kGroups) {
+            const int s = i % kStages;
+            const uint32_t par = static_cast<uint32_t>((i / kStages) & 1);
+    #ifdef GBTOPK_TRACE
+            unsigned long long t_a = clock64();
+            t_busy += t_a - t_mark;
+    #endif
+            // a stage the producer never filled must not be read, nor its
+            // metadata: on a timeout or an abort the warp stops, and the
+            // finalize kernel recomputes every row of the call from global memory
+            int got = 0;
+            if (lane == 0) got = mbar_wait_or_abort(&c.full[s], par, p.wait_polls, &c.abort_flag);
+            got = __shfl_sync(0xffffffffu, got, 0);
+    #ifdef GBTOPK_TRACE
+            t_mark = clock64();
+            t_wait += t_mark - t_a;
+            ++n_items;
+    #endif
+            if (got != 1) {
+                if (got == 0 && lane == 0) {
+                    atomicExch(&c.abort_flag, 1u);
+                    atomicOr(reinterpret_cast<uint32_t *>(p.ws), kStatusWaitTimeout);
+                    reinterpret_cast<volatile uint32_t *>(p.ws)[1] = 1u;
+                }
+                break;
+            }
+            mbar_wait(&c.full[s], par);  // completes at once: acquire for every lane
+            const StageMeta m = meta[s];
+            const int64_t grow = p.row0 + m.row;
+            const int nvec = ((m.off + m.len) * es + 15) >> 4;
+            const uint4 *svec = reinterpret_cast<const uint4 *>(stages + static_cast<size_t>(s) * kStageBytes);
+            const int vbase = gw * 32 + static_cast<int>(lane);
+            uint4 w[VPL];
+    #pragma unroll
             for (int j = 0; j < VPL; ++j) {
                 const int v = vbase + j * kGroupWarps * 32;
                 w[j] = v < nvec ? svec[v] : make_uint4(0, 0, 0, 0);
             }
-        }
-        if (!ok) {
+            const PassTest<DT> pass(rf[m.row].t_lo);
+            uint32_t msk[VPL];
+            uint32_t cnt = 0;
+    #pragma unroll
+            for (int j = 0; j < VPL; ++j) {
+                const int v = vbase + j * kGroupWarps * 32;
+                uint32_t bits = pass.mask(w[j]);
+                if (v == 0 || v >= nvec - 1) bits &= valid_lanes<EPV>(v, nvec, m.off, m.len);
+                msk[j] = bits;
+                cnt += __popc(bits);
+            }
+            // warp-level slot reservation; the same atomic counts the warps done
+            uint32_t incl = cnt;
+    #pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= static_cast<uint32_t>(o)) incl += y;
+            }
+            const uint32_t wtotal = __shfl_sync(0xffffffffu, incl, 31);
+            unsigned long long old = 0;
+            if (lane == 0) old = atomicAdd(&c.scombo[par][s], (1ull << 32) | wtotal);
+            const uint32_t base = __shfl_sync(0xffffffffu, static_cast<uint32_t>(old), 0);
+            if (lane == 0 && static_cast<uint32_t>(old >> 32) == kGroupWarps - 1) {  // last warp on the chunk
+                row_counts(p, grow)[m.chunk] = base + wtotal;
+                c.scombo[par][s] = 0;
+            }
+            uint32_t slot = base + incl - cnt;
+            const uint32_t cap = static_cast<uint32_t>(m.seg_cap);
+            uint2 *seg = row_segs(p, grow) + static_cast<int64_t>(m.chunk) * m.seg_cap;
+            const int colbase = static_cast<int>(m.c0) - m.off;
+            // the lane's pass bits in one mask (bit EPV * j + q), then one
+            // iteration per candidate: its value is read back from the stage,
+            // which this warp releases only afterwards
+            constexpr int NW = (VPL * EPV + 31) / 32;
+            uint32_t mw[NW];
+    #pragma unroll
+            for (int wd = 0; wd < NW; ++wd) mw[wd] = 0;
+    #pragma unroll
+            for (int j = 0; j < VPL; ++j) mw[(j * EPV) / 32] |= msk[j] << ((j * EPV) % 32);
+            const raw_t *selem = reinterpret_cast<const raw_t *>(svec);
+    #pragma unroll
+            for (int wd = 0; wd < NW; ++wd) {
+                uint32_t bits = mw[wd];
+                while (bits) {
+                    const int e = wd * 32 + __ffs(bits) - 1;
+                    bits &= bits - 1;
+                    const int epos = (vbase + (e / EPV) * kGroupWarps * 32) * EPV + (e % EPV);
+                    if (slot < cap) seg[slot] = make_uint2(static_cast<uint32_t>(selem[epos]),
+                                                           static_cast<uint32_t>(colbase + epos));
+                    ++slot;
+                }
+            }
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&c.empty[s]);
-                atomicOr(reinterpret_cast<uint32_t *>(p.ws), kStatusWaitTimeout);
-                row_counts(p, grow)[m.chunk] = 0xFFFFFFFFu;  // finalize recomputes the row
-            }
-            continue;
+            if (lane == 0) mbar_arrive(&c.empty[s]);  // release: this warp's reads of the stage are done
         }
-        const PassTest<DT> pass(rf[m.row].t_lo);
-        uint32_t msk[VPL];
-        uint32_t cnt = 0;
-#pragma unroll
-        for (int j = 0; j < VPL; ++j) {
-            const int v = vbase + j * kGroupWarps * 32;
-            uint32_t bits = pass.mask(w[j]);
-            if (v == 0 || v >= nvec - 1) bits &= valid_lanes<EPV>(v, nvec, m.off, m.len);
-            msk[j] = bits;
-            cnt += __popc(bits);
+    #ifdef GBTOPK_TRACE
+        t_busy += clock64() - t_mark;
+        if (threadIdx.x == 32 && kTraceBase + blockIdx.x < kTraceBlocks) {
+            g_trace[kTraceBase + blockIdx.x][8] = t_wait;
+            g_trace[kTraceBase + blockIdx.x][9] = t_busy;
+            g_trace[kTraceBase + blockIdx.x][10] = n_items;
+            unsigned long long t_;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));
+            g_trace[kTraceBase + blockIdx.x][11] = t_;
         }
-        // warp-level slot reservation; the same atomic counts the warps done
-        uint32_t incl = cnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= static_cast<uint32_t>(o)) incl += y;
-        }
-        const uint32_t wtotal = __shfl_sync(0xffffffffu, incl, 31);
-        unsigned long long old = 0;
-        if (lane == 0) old = atomicAdd(&c.scombo[par][s], (1ull << 32) | wtotal);
-        const uint32_t base = __shfl_sync(0xffffffffu, static_cast<uint32_t>(old), 0);
-        if (lane == 0 && static_cast<uint32_t>(old >> 32) == kGroupWarps - 1) {  // last warp on the chunk
-            row_counts(p, grow)[m.chunk] = base + wtotal;
-            c.scombo[par][s] = 0;
-        }
-        uint32_t slot = base + incl - cnt;
-        const uint32_t cap = static_cast<uint32_t>(m.seg_cap);
-        uint2 *seg = row_segs(p, grow) + static_cast<int64_t>(m.chunk) * m.seg_cap;
-        const int colbase = static_cast<int>(m.c0) - m.off;
-        // the lane's pass bits in one mask (bit EPV * j + q), then one
-        // iteration per candidate: its value is read back from the stage,
-        // which this warp releases only afterwards
-        constexpr int NW = (VPL * EPV + 31) / 32;
-        uint32_t mw[NW];
-#pragma unroll
-        for (int wd = 0; wd < NW; ++wd) mw[wd] = 0;
-#pragma unroll
-        for (int j = 0; j < VPL; ++j) mw[(j * EPV) / 32] |= msk[j] << ((j * EPV) % 32);
-        const raw_t *selem = reinterpret_cast<const raw_t *>(svec);
-#pragma unroll
-        for (int wd = 0; wd < NW; ++wd) {
-            uint32_t bits = mw[wd];
-            while (bits) {
-                const int e = wd * 32 + __ffs(bits) - 1;
-                bits &= bits - 1;
-                const int epos = (vbase + (e / EPV) * kGroupWarps * 32) * EPV + (e % EPV);
-                if (slot < cap) seg[slot] = make_uint2(static_cast<uint32_t>(selem[epos]),
-                                                       static_cast<uint32_t>(colbase + epos));
-                ++slot;
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&c.empty[s]);  // release: this warp's reads of the stage are done
+    #endif
     }
-#ifdef GBTOPK_TRACE
-    t_busy += clock64() - t_mark;
-    if (threadIdx.x == 32 && kTraceBase + blockIdx.x < kTraceBlocks) {
-        g_trace[kTraceBase + blockIdx.x][8] = t_wait;
-        g_trace[kTraceBase + blockIdx.x][9] = t_busy;
-        g_trace[kTraceBase + blockIdx.x][10] = n_items;
-        unsigned long long t_;
-        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));
-        g_trace[kTraceBase + blockIdx.x][11] = t_;
+    // every warp is done with the ring: if a wait gave up, the finalize
+    // kernel recomputes every row of this call, and the latest copy into
+    // each stage must land before the block leaves (bounded wait; its phase
+    // is the stage's latest)
+    __syncthreads();
+    if (threadIdx.x == 0 && c.abort_flag) {
+        reinterpret_cast<volatile uint32_t *>(p.ws)[1] = 1u;
+        const int64_t issued = c.bcast[0];
+        for (int64_t i = issued - kStages < 0 ? 0 : issued - kStages; i < issued; ++i)
+            if (!mbar_wait(&c.full[i % kStages], static_cast<uint32_t>((i / kStages) & 1)))
+                atomicOr(reinterpret_cast<uint32_t *>(p.ws), kStatusCopyLost);
     }
-#endif
+    GBTOPK_TRACE_POINT(6, 0);
 }
+
 
 // Finalize kernel: one block per split row.  The row's chunk segments
 // (L2-resident) are gathered into shared memory by one bulk copy per chunk
@@ -1781,7 +1831,7 @@ struct FinalRegion {
 template <int DT, int NT>
 __device__ void finalize_row(const Params &p, int64_t row, int64_t n, int64_t col0, int64_t nch,
                              const FinalRegion &fr, unsigned long long *bar, uint32_t parity, bool ws_hist,
-                             Ctrl &c, int64_t trace_idx) {
+                             bool recompute, Ctrl &c, int64_t trace_idx) {
     (void)trace_idx;  // the trace row of this block (GBTOPK_TRACE builds)
     using raw_t = typename Elem<DT>::raw_t;
     static_assert(NT >= kCoarseBins, "one coarse bin per thread");
@@ -1821,7 +1871,7 @@ __device__ void finalize_row(const Params &p, int64_t row, int64_t n, int64_t co
     uint32_t total_p;
     const uint32_t poff = block_excl_scan(padded, c, total_p);  // its barriers publish the flags
     const uint32_t total = total_p - c.cand_count;
-    bool fallback = c.bcast[5] != 0 || total < static_cast<uint32_t>(k);
+    bool fallback = recompute || c.bcast[5] != 0 || total < static_cast<uint32_t>(k);
     const bool in_smem = total_p <= fr.gather_cap;
     const bool gathered = !fallback && in_smem;  // block-uniform
     bool copy_ok = true;
@@ -1841,7 +1891,7 @@ __device__ void finalize_row(const Params &p, int64_t row, int64_t n, int64_t co
                 "l"(segs + static_cast<int64_t>(tid) * cap), "r"(padded * 8u), "r"(smem_u32(bar))
                 : "memory");
         }
-        copy_ok = wait_bar(p.ws, c, bar, parity);
+        copy_ok = wait_bar(p.ws, c, bar, parity, p.wait_polls);
         if (tid == 0) GBTOPK_TRACE_SET(trace_idx, 9, -1);
         if (copy_ok) {
             if (tid < nch && (cnt & 1u)) fr.cand[poff + cnt].y = kPadColumn;
@@ -2047,7 +2097,10 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
     if (threadIdx.x == 0) mbar_init(&c.bar);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     GBTOPK_TRACE_POINT(0, 0);
-    finalize_row<DT, kFinalThreads>(p, row, n, col0, nch, fr, &c.bar, 0, false, c, kTraceFinal + blockIdx.x);
+    // a stream block that gave up left some chunks unfiltered: recompute
+    const bool aborted = __ldcg(reinterpret_cast<const uint32_t *>(p.ws) + 1) != 0u;
+    finalize_row<DT, kFinalThreads>(p, row, n, col0, nch, fr, &c.bar, 0, false, aborted, c,
+                                    kTraceFinal + blockIdx.x);
     GBTOPK_TRACE_POINT(6, 0);
 }
 
@@ -2104,7 +2157,7 @@ __global__ void __launch_bounds__(kThreads, 3) chunk_kernel(const __grid_constan
     const uint2 guess = __ldcg(reinterpret_cast<const uint2 *>(info));  // t_lo, bin shift
     if (tid == 0) c.sel_count = 0;
     c.rhist[tid] = 0;  // the chunk's coarse candidate histogram (kThreads == kCoarseBins)
-    const bool ok = wait_bar(p.ws, c, &c.bar, 0);
+    const bool ok = wait_bar(p.ws, c, &c.bar, 0, p.wait_polls);
     GBTOPK_TRACE_POINT(2, 0);
     if (ok) {
         const int nvec = ((sp.off + len) * es + 15) >> 4;
@@ -2207,7 +2260,7 @@ __global__ void __launch_bounds__(kThreads, 3) chunk_kernel(const __grid_constan
     fr.cand = reinterpret_cast<uint2 *>(stage + kFusedOffCand);
     fr.gather_cap = kFusedGatherCap;
     fr.scratch = stage;  // det_scratch_bytes(2048) = 40 KB, below the selection
-    finalize_row<DT, kThreads>(p, row, n, col0, nch, fr, &c.bar, 1, true, c, kTraceChunk + blockIdx.x);
+    finalize_row<DT, kThreads>(p, row, n, col0, nch, fr, &c.bar, 1, true, false, c, kTraceChunk + blockIdx.x);
 }
 
 // ---------------------------------------------------------------- small rows
