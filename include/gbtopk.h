@@ -95,9 +95,11 @@ extern "C" {
  *  workspace    device scratch of at least gbtopk_workspace_bytes(...) bytes,
  *               256-byte aligned.  Its first 4 bytes are a status word that
  *               should start at zero (see gbtopk_device_status); everything
- *               else is scratch that each call writes before reading, so the
- *               contents need no initialisation and one workspace serves any
- *               sequence of calls on one stream.  Calls that may overlap in
+ *               else is scratch that each call writes before reading (the
+ *               row's guess, chunk ticket and candidate counters are written
+ *               by the call's first kernel), so the contents need no
+ *               initialisation and one workspace serves any sequence of
+ *               calls on one stream.  Calls that may overlap in
  *               time (different streams, concurrent graph replays) need
  *               separate workspaces.
  *  stream       cudaStream_t.
@@ -214,10 +216,19 @@ size_t gbtopk_workspace_bytes(int64_t num_rows, int64_t width, int32_t top_k, in
 
 /*
  * gbtopk_device_status — reads (and clears) the device status word of a
- * workspace.  Synchronises `stream`.  *flags receives a bit set: bit 0 = a
- * bounded wait on an asynchronous copy gave up (the affected rows were then
- * recomputed from global memory, so outputs stay exact).  Returns GBTOPK_OK,
- * GBTOPK_EINVAL or GBTOPK_ECUDA.
+ * workspace.  Synchronises `stream`.  *flags receives a bit set:
+ *   bit 0  a bounded wait on an asynchronous copy gave up; the affected rows
+ *          (on the three-kernel path: every row of that call) were
+ *          recomputed from global memory, so the outputs are exact;
+ *   bit 1  a copy did not land even within a second bounded wait: the
+ *          outputs of that call are not reliable (the shared memory the copy
+ *          targets was not reused; rows whose selection needed it were left
+ *          unwritten or written unsorted).
+ * The waits are bounded by a poll count; the environment variable
+ * GBTOPK_WAIT_POLLS (a positive integer, read once per process) lowers the
+ * first wait's count, which exercises the recovery of bit 0 in tests.
+ * Returns GBTOPK_OK, GBTOPK_EINVAL or GBTOPK_ECUDA.  The pages define no
+ * such call.
  */
 int gbtopk_device_status(void *workspace, uint32_t *flags, void *stream);
 
@@ -256,12 +267,15 @@ int gbtopk_plan_query(int64_t num_rows, int64_t width, int32_t top_k, int dtype,
  * example a 64 x 163840 fp32 batch with top_k 2048 needs about 6.3 MiB.
  *
  * The first call on a device looks up the buffer's device address (once per
- * device); make that first call before capturing a CUDA graph.  All calls
- * on a device share the one buffer and its contents carry over between
- * calls (nothing needs clearing: each call writes the scratch it reads), so
- * calls that may overlap in time on the GPU — other streams, concurrent
- * graph replays, other host threads — race on it and must be serialised by
- * the caller.
+ * device); make that first call before capturing a CUDA graph.  The address
+ * belongs to the device's context: after cudaDeviceReset the process must
+ * not call this entry point again.  All calls on a device share the one
+ * buffer and its contents carry over between calls (nothing needs clearing:
+ * each call writes the scratch it reads), so calls that may overlap in time
+ * on the GPU — other streams, concurrent graph replays, other host threads —
+ * race on it and must be serialised by the caller.  The buffer's device
+ * status word (see gbtopk_device_status) cannot be read on this path: the
+ * bounded-wait flags of these calls are not reported.
  */
 int gbtopk_varlen_static_ws(const void *logits, int dtype, int64_t num_rows, int64_t width,
                             int64_t row_stride, const int32_t *seq_lens, int32_t next_n,
@@ -269,7 +283,9 @@ int gbtopk_varlen_static_ws(const void *logits, int dtype, int64_t num_rows, int
                             int32_t *out_indices, void *out_values, int deterministic,
                             void *stream);
 
-/* Human-readable name of a status code (static string). */
+/* Human-readable name of a status code (static string).  The pages define no
+ * such call; the codes follow the error cases of the FlashInfer
+ * `top_k_varlen` page ("Raises") and the status convention above. */
 const char *gbtopk_status_str(int status);
 
 #ifdef __cplusplus

@@ -1,33 +1,35 @@
 // Device code of gbtopk: batched variable-length exact top-K on sm_103a.
 //
-// One launch serves a whole ragged batch.  Block b handles chunk b % C of
-// row b / C (C = chunks per row, fixed by the launch plan from the buffer
-// width only, so the geometry never depends on seq_lens contents and the
-// call is CUDA-graph safe; TensorRT-LLM PR #17821, run_varlen commits).
-//
-// Per row (valid length n, from the FlashInfer `top_k_varlen` seq_lens
-// formula or from the page-table call's lengths / row_starts):
-//   * n == 0            -> all -1 (zero-window rows).
-//   * n <= k            -> every valid column, then -1 (short path).
-//   * k < n <= chunk    -> the row is staged in shared memory by one bulk
-//                          asynchronous copy and an exact radix select runs
-//                          on it (8-bit digits, shared-memory histograms with
-//                          warp-aggregated atomics).
-//   * n > chunk         -> split: each block stages its chunk, guesses a
-//                          threshold from a strided sample of the row (the
-//                          self-sampling guess of TensorRT-LLM PR #17821,
-//                          optionally anchored at the hint's argmax), keeps
-//                          the candidates at or above it with a histogram of
-//                          their keys, and publishes both to the workspace.
-//                          The last block of the row (atomic ticket) finds
-//                          the exact k-th key from the histogram and the
-//                          candidates, and restores the workspace to zero.
-//                          If the guess was too high or a buffer overflowed
-//                          (count-crossing check), that block recomputes the
-//                          row with the exact select from global memory, so
-//                          the result never depends on the guess.
-// Ranking uses order-preserving integer keys (signed zeros equal; +-inf and
-// denormals exact), so no float compare depends on flush-to-zero.
+// Every call's launch geometry depends only on (rows, width, top_k, dtype),
+// never on the seq_lens / lengths contents, so any call can be captured in a
+// CUDA graph and replayed with new lengths (TensorRT-LLM PR #17821, the
+// run_varlen commits).  Per row (valid length n, from the FlashInfer
+// `top_k_varlen` seq_lens formula or from the page-table calls' lengths and
+// row_starts):
+//   * n == 0 or n <= k -> every valid column, then -1 (short path);
+//   * widths up to 2048 without the sorted order: one warp per row
+//     (small_kernel, a warp-private radix select on keys in registers);
+//   * widths up to two 32 KB chunks: one block per row (row_kernel): the
+//     row is staged in shared memory by one bulk copy, a threshold is
+//     guessed from a strided sample, the elements at or above it are kept
+//     and selected exactly in shared memory;
+//   * longer rows (split plans), top_k <= 2048 and batches of at most 2048
+//     (row, 64 KB chunk) slots: row_kernel makes each row's guess (the
+//     self-sampling guess of TensorRT-LLM PR #17821, its key range widened
+//     to the hint's argmax), then chunk_kernel runs one block per chunk:
+//     the chunk is filtered against the guess into a candidate segment and
+//     the row's last block (atomic ticket) selects the row in its own
+//     shared memory (finalize_row);
+//   * other split plans: row_kernel's guesses, then the persistent
+//     stream_kernel filters every chunk through a bulk-copy ring, then
+//     final_kernel selects each row (finalize_row).
+// The three launches of a call are chained by programmatic dependent launch.
+// A guess that was too high, a candidate segment that overflowed or a
+// bounded wait that gave up sends the row through an exact radix select
+// over global memory (count-crossing check), so the result never depends on
+// the guess.  Ranking uses order-preserving integer keys (signed zeros
+// equal; +-inf and denormals exact), so no float compare depends on
+// flush-to-zero.
 #include <cstdint>
 #include <map>
 #include <mutex>
@@ -1596,18 +1598,9 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
 }
 
 
-// Finalize kernel: one block per split row.  The row's chunk segments
-// (L2-resident) are gathered into shared memory by one bulk copy per chunk
-// (each segment padded to an even count so every copy starts on a 16-byte
-// boundary; the padding slot is marked with column 0xFFFFFFFF), then the
-// candidates' keys are histogrammed over kBins bins above the guess, the bin
-// holding the k-th key is found, every candidate of a higher bin is kept and
-// the boundary bin's members are ranked exactly.  Rows with more candidates
-// than the shared buffer holds make the same two passes straight over the
-// segments in L2.  Falls back to an exact radix select over the row in
-// global memory when a segment overflowed, the guess was too high or the
-// boundary bin is too crowded.
-struct SegMap {  // candidate j of the concatenated segments -> its address
+// Candidate j of a split row's concatenated chunk segments -> its address
+// (the finalize's passes over segments left in L2).
+struct SegMap {
     const uint2 *segs;
     const uint32_t *choff;  // first candidate number of each chunk
     int nch;
@@ -2070,6 +2063,9 @@ __device__ void finalize_row(const Params &p, int64_t row, int64_t n, int64_t co
     if (tid == 0) GBTOPK_TRACE_SET(trace_idx, 12, -1);
 }
 
+// Finalize kernel (split plans of the three-kernel path): one block per
+// split row, after the stream kernel has filtered every chunk; the row is
+// selected by finalize_row in this block's shared memory.
 template <int DT>
 __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(128) uint8_t smem[];

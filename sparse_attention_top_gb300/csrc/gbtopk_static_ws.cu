@@ -35,7 +35,9 @@ void *g_dev_ptr[kMaxDevices] = {};
 
 // Device address of g_static_ws on the current device, looked up once per
 // device (the host-side symbol is only a handle; the kernels need the
-// address the runtime assigned on that device).
+// address the runtime assigned on that device).  The cached address belongs
+// to the device's current context: after cudaDeviceReset it is stale, so
+// this entry point must not be used again in that process.
 int static_ws_address(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return GBTOPK_ECUDA;
@@ -59,11 +61,13 @@ int gbtopk_varlen_static_ws(const void *logits, int dtype, int64_t num_rows, int
                             int32_t compress_ratio, int32_t top_k, const int32_t *pre_idx,
                             int32_t *out_indices, void *out_values, int deterministic,
                             void *stream) {
-    // Refuse, before touching the device, any geometry whose scratch does
-    // not fit in the built-in buffer.
-    const size_t need = gbtopk_workspace_bytes(num_rows, width, top_k, dtype);
-    if (need == 0) return top_k > GBTOPK_MAX_TOP_K ? GBTOPK_EUNSUPPORTED : GBTOPK_EINVAL;
-    if (need > kStaticWsBytes) return GBTOPK_EWORKSPACE;
+    // Refuse, before touching the device, a geometry the library does not
+    // plan (with gbtopk_varlen's own status) or whose scratch does not fit
+    // in the built-in buffer.
+    int64_t plan[13];
+    const int prc = gbtopk_plan_query(num_rows, width, top_k, dtype, plan);
+    if (prc != GBTOPK_OK) return prc;
+    if (static_cast<size_t>(plan[8]) > kStaticWsBytes) return GBTOPK_EWORKSPACE;
     void *ws = nullptr;
     const int rc = static_ws_address(&ws);
     if (rc != GBTOPK_OK) return rc;

@@ -228,3 +228,24 @@ def _cu(**kw):
 ])
 def test_cu_seqlens_argument_checks(kw, status):
     assert _cu(**kw) == status
+
+
+@pytest.mark.parametrize("num_rows,width,top_k,dtype,status", [
+    (4, 1 << 31, 8, 0, gb.EUNSUPPORTED),          # width beyond the plan (int32 columns)
+    (4, 100, 0, 0, gb.EINVAL),
+    (4, 100, gb.MAX_TOP_K + 1, 0, gb.EUNSUPPORTED),
+    (4, 100, 8, 7, gb.EINVAL),                    # unknown dtype
+    (4, 4 * 16384 * 256 + 1, 8, 0, gb.EUNSUPPORTED),  # wider than the split plan allows
+    (1024, 262144, 2048, 0, gb.EWORKSPACE),       # more scratch than the built-in buffer
+])
+def test_static_scratch_refusals_match_the_plan(num_rows, width, top_k, dtype, status):
+    """The allocation-free entry point refuses a geometry before touching the
+    device, with the status gbtopk_varlen's plan gives (or EWORKSPACE when
+    the built-in scratch is too small)."""
+    lib = gb.load_library()
+    st = lib.gbtopk_varlen_static_ws(A, dtype, num_rows, width, width, A + 4096, 1, 1, top_k, None,
+                                     A + 8192, None, 0, None)
+    assert st == status
+    if status != gb.EWORKSPACE:
+        assert _varlen(num_rows=num_rows, width=width, row_stride=width, top_k=top_k,
+                       dtype=dtype) == status

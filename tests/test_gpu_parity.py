@@ -4,7 +4,7 @@ Covers the five workloads (reduced and at full size), the split / direct /
 short / empty row paths, ties, signed zeros, infinities, denormals, poisoned
 padding (TensorRT-LLM PR #17821, "padding poisoned with 3e38"), misaligned and
 strided score views, degenerate hints, deterministic mode, the compact
-page-table transform, output canaries, workspace self-restoration and CUDA
+page-table transform, output canaries, a poisoned scratch workspace and CUDA
 graph replay with changing lengths.
 """
 import warnings
