@@ -30,7 +30,7 @@ def main():
     assert bench.reduce_sum(float(rows)) == 128.0
     bench.barrier()
     # each rank's batch is seeded by its rank, so the ranks' inputs differ
-    case = bench.make_case("dsv32_decode", rank)
+    case = bench._varlen_case("dsv32_decode", rank)
     assert tuple(case.logits.shape) == (64, 163840) and case.top_k == 2048
     sig = float(case.logits[:, :256].double().sum())
     sigs = [None, None]

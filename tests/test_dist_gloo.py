@@ -54,3 +54,25 @@ def test_reference_arm_prints_once_on_rank0():
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_gpus_flag_starts_its_own_ranks():
+    """`bench.py --gpus 2` started without a launcher runs two ranks itself
+    (through torch.distributed.run); the reference arm then prints one line
+    from rank 0 with n_gpus 2."""
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="", OMP_NUM_THREADS="1")
+    for key in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        env.pop(key, None)
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2",
+                        "--steps", "1", "--warmup", "0"], cwd=ROOT, env=env, capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1 and lines[0]["n_gpus"] == 2 and lines[0]["impl"] == "reference"
+
+
+def test_gpus_flag_must_match_the_launcher():
+    """Under a launcher, --gpus must equal WORLD_SIZE (no silent n_gpus 1)."""
+    r = _torchrun(["bench.py", "--impl", "reference", "--gpus", "4", "--steps", "1",
+                   "--warmup", "0"])
+    assert r.returncode != 0 and "WORLD_SIZE" in (r.stdout + r.stderr)
