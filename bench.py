@@ -52,6 +52,7 @@ L2_BYTES = 129 * 1024 * 1024
 # workload and the SHA-256 prefix of the kernel source it was taken on;
 # reported as null once the kernel source changes.
 NCU_TRAFFIC = {
+    ("dsv32_decode", "fbad71a0f3b45217"): 21_873_664,   # row 2,364,672 + chunk 19,508,992
 }
 
 
@@ -66,6 +67,8 @@ def parse():
     ap.add_argument("--extra-steps", type=int, default=50,
                     help="timed steps of each of the other workloads")
     ap.add_argument("--no-extra", action="store_true", help="time the headline workload only")
+    ap.add_argument("--sweep-rows", type=int, default=1024,
+                    help="rows of the long-row sweep (a smaller batch for profiler captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true",
@@ -133,6 +136,9 @@ def reduce_sum(x: float) -> float:
 
 # ------------------------------------------------------------------ workloads
 
+SWEEP_ROWS = [1024]   # --sweep-rows
+
+
 def _varlen_case(name: str, rank: int):
     import workloads
     s = 17 * rank
@@ -141,7 +147,7 @@ def _varlen_case(name: str, rank: int):
     if name == "dsv32_decode_nohint":
         return workloads.dsv32_decode(hinted=False, seed=2000 + s)
     if name == "long_row_sweep_1024":
-        return workloads.long_row_sweep(1024, 2048, True, seed=3999 + s)
+        return workloads.long_row_sweep(SWEEP_ROWS[0], 2048, True, seed=3999 + s)
     if name == "dsv4_mtp":
         return workloads.dsv4_mtp(seed=4000 + s)
     if name == "short_rows":
@@ -607,6 +613,7 @@ def run_e2e(case, dev, args, gb):
 
 def main():
     args = parse()
+    SWEEP_ROWS[0] = args.sweep_rows
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
         sys.exit(spawn_ranks(args.gpus))
     rank, world, local = dist_init(args.gpus)
