@@ -18,6 +18,7 @@ constexpr int kBinBits = 12;
 constexpr int kBins = 1 << kBinBits;   // candidate histogram bins
 constexpr int kGuessBins = 512;        // bins of each round of the sample's threshold search
 constexpr int kRankMax = 256;          // boundary-bin size resolved by rank counting
+constexpr int kRankAllMax = 64;        // the same in the finalize (a block radix select above)
 constexpr size_t kCtrlBytes = 2048;    // per-block control block (counters, scan, digit histogram)
 constexpr int kChunkBytes = 32768;     // bytes per stream chunk (one bulk copy)
 constexpr int kStages = 6;             // bulk-copy ring depth of the stream kernel

@@ -53,7 +53,7 @@ constexpr int kTraceChunk = 8192;  // chunk kernel blocks (up to 24576 of them)
 // Phase timestamps (%globaltimer, ns) of the first kTraceBlocks blocks, for
 // builds compiled with -DGBTOPK_TRACE (read back by gbtopk_trace_read).
 constexpr int kTraceBlocks = 1 << 16;
-__device__ unsigned long long g_trace[kTraceBlocks][16];
+__device__ unsigned long long g_trace[kTraceBlocks][32];
 // Each kernel declares kTraceBase: its blocks use g_trace[kTraceBase + block].
 #define GBTOPK_TRACE_POINT(slot, value)                                                      \
     do {                                                                                     \
@@ -922,8 +922,10 @@ __device__ uint32_t adaptive_threshold(const uint32_t *keys, int m, uint32_t r, 
     __syncthreads();
     for (int i = threadIdx.x; i < m; i += NT) atomicAdd(&hist[(keys[i] - kmin) >> shift], 1u);
     __syncthreads();
+    if (threadIdx.x == 0) GBTOPK_TRACE_SET(blockIdx.x, 16, -1);  // (row kernel blocks)
     warp_find_two_bins<NB>(hist, e, r, c);
     __syncthreads();
+    if (threadIdx.x == 0) GBTOPK_TRACE_SET(blockIdx.x, 17, -1);
     const uint32_t be = c.bcast[2];
     upper_e = kmin + (be << shift) + ((1u << shift) - 1u);
     if (upper_e < kmin || upper_e > kmax) upper_e = kmax;  // the top bin may reach past kmax
@@ -940,6 +942,7 @@ __device__ uint32_t adaptive_threshold(const uint32_t *keys, int m, uint32_t r, 
         if ((d >> shift) == b) atomicAdd(&hist[(d - (b << shift)) >> shift2], 1u);
     }
     __syncthreads();
+    if (threadIdx.x == 0) GBTOPK_TRACE_SET(blockIdx.x, 18, -1);
     warp_find_two_bins<NB>(hist, rem, rem, c);
     __syncthreads();
     return edge + (c.bcast[2] << shift2);
@@ -1014,6 +1017,45 @@ __device__ uint32_t filter_staged(const void *stage, int off, int len, int col_b
     return total;
 }
 
+// Places the best `need` of the bsize members of blist (shared memory) at
+// sel[above + rank], rank being the member's position in the total order
+// (key desc, then the tie mode's column order; smaller columns first for
+// tie mode 0), which no two members share.  Each member's order is packed
+// into one 64-bit composite (key above, complemented tie column below),
+// blist is overwritten with the composites, and each member is ranked by
+// counting the composites above its own.  All threads; ends with a barrier.
+template <int DT>
+__device__ void rank_all(uint2 *blist, uint32_t bsize, uint32_t need, uint32_t above, int tie, uint2 *sel) {
+    unsigned long long *comp = reinterpret_cast<unsigned long long *>(blist);
+    constexpr int kMaxPer = 4;  // members per thread (bsize <= 4 * blockDim.x)
+    uint2 me[kMaxPer];
+    unsigned long long mine[kMaxPer];
+#pragma unroll
+    for (int q = 0; q < kMaxPer; ++q) {
+        const uint32_t i = threadIdx.x + q * blockDim.x;
+        me[q] = i < bsize ? blist[i] : make_uint2(0u, 0u);
+        mine[q] = (static_cast<unsigned long long>(Elem<DT>::key(me[q].x)) << 32) | ~tie_key(me[q].y, tie);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < kMaxPer; ++q) {
+        const uint32_t i = threadIdx.x + q * blockDim.x;
+        if (i < bsize) comp[i] = mine[q];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < kMaxPer; ++q) {
+        const uint32_t i = threadIdx.x + q * blockDim.x;
+        if (i < bsize) {
+            uint32_t rank = 0;
+#pragma unroll 4
+            for (uint32_t j = 0; j < bsize; ++j) rank += comp[j] > mine[q] ? 1u : 0u;
+            if (rank < need) sel[above + rank] = me[q];
+        }
+    }
+    __syncthreads();
+}
+
 // Finds the exact top-k among `total` (>= k) candidates whose keys are
 // counted in hist[kBins] (shared memory): the bin b* holding the k-th key
 // from the top, every candidate of a higher bin, and the best `need` of bin
@@ -1045,20 +1087,7 @@ __device__ bool select_from_candidates(const CandSrc &cands, uint32_t total, con
     __syncthreads();
     const uint32_t need = static_cast<uint32_t>(k) - above;
     if (bsize <= kRankMax) {
-        // rank every member of bin b* against the others: a total order by
-        // (key desc, column asc); the first `need` ranks are selected
-        for (uint32_t i = threadIdx.x; i < bsize; i += blockDim.x) {
-            const uint2 me = blist[i];
-            const uint32_t mk = Elem<DT>::key(me.x);
-            uint32_t rank = 0;
-            for (uint32_t j = 0; j < bsize; ++j) {
-                const uint2 o = blist[j];
-                const uint32_t ok = Elem<DT>::key(o.x);
-                rank += (ok > mk || (ok == mk && tie_key(o.y, tie) < tie_key(me.y, tie))) ? 1u : 0u;
-            }
-            if (rank < need) sel[above + rank] = me;
-        }
-        __syncthreads();
+        rank_all<DT>(blist, bsize, need, above, tie, sel);
     } else {
         const PairSrc<DT> bs{blist};
         uint32_t t, gt;
@@ -1766,7 +1795,9 @@ __device__ void select_members(const uint2 *blist, uint32_t bsize, uint32_t need
 template <int DT, int NT>
 __device__ bool rank_boundary(const uint2 *blist, uint32_t bsize, uint32_t need, uint32_t above, int tie,
                               uint2 *sel, Ctrl &c) {
-    if (bsize <= static_cast<uint32_t>(NT)) {
+    if (bsize <= static_cast<uint32_t>(kRankAllMax)) {
+        rank_all<DT>(const_cast<uint2 *>(blist), bsize, need, above, tie, sel);
+    } else if (bsize <= static_cast<uint32_t>(NT)) {
         select_members<NT>(blist, bsize, need, above, tie, sel, c, [](uint32_t raw) { return Elem<DT>::key(raw); });
     } else {
         constexpr int KB = Elem<DT>::kKeyBits;
@@ -1987,9 +2018,10 @@ __device__ void finalize_row(const Params &p, int64_t row, int64_t n, int64_t co
             if (in_smem && total_p <= static_cast<uint32_t>(RC * NT)) {
                 // the gathered candidates stay in shared memory: mark, then
                 // revisit only the marked ones
+                const int nu = static_cast<int>((total_p + NT - 1) / NT);  // (block-uniform)
                 uint32_t hm = 0, em = 0;
 #pragma unroll 8
-                for (int u = 0; u < RC; ++u) {
+                for (int u = 0; u < nu; ++u) {
                     const uint32_t i = u * NT + tid;
                     if (i < total_p) {
                         bool hi, eq;
@@ -1998,8 +2030,10 @@ __device__ void finalize_row(const Params &p, int64_t row, int64_t n, int64_t co
                         em |= static_cast<uint32_t>(eq) << u;
                     }
                 }
+                if (tid == 0) GBTOPK_TRACE_SET(trace_idx, 19, -1);
                 uint32_t ptot;
                 const uint32_t pre = block_excl_scan((static_cast<uint32_t>(__popc(hm)) << 16) | __popc(em), c, ptot);
+                if (tid == 0) GBTOPK_TRACE_SET(trace_idx, 20, -1);
                 uint32_t hs = pre >> 16, es = pre & 0xFFFFu;
                 while (hm) {
                     const int u = __ffs(hm) - 1;
@@ -2011,6 +2045,7 @@ __device__ void finalize_row(const Params &p, int64_t row, int64_t n, int64_t co
                     em &= em - 1;
                     fr.blist[es++] = fr.cand[u * NT + tid];
                 }
+                if (tid == 0) GBTOPK_TRACE_SET(trace_idx, 21, -1);
             } else {
                 uint32_t nhi = 0, neq = 0;
                 for_each_cand([&](bool live, uint2 v) {
@@ -2044,6 +2079,7 @@ __device__ void finalize_row(const Params &p, int64_t row, int64_t n, int64_t co
     // the next call's first kernel may launch now (it waits for this grid
     // to complete before reading anything)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (tid == 0) GBTOPK_TRACE_SET(trace_idx, 15, -1);
     bool scratch_ok = true;
     if (!copy_ok) {  // the sorted output's scratch overlaps the gather region
         if (tid == 0) {
@@ -2219,11 +2255,14 @@ __global__ void __launch_bounds__(kThreads, 3) chunk_kernel(const __grid_constan
     // bin), then the ticket: the barriers and thread 0's fence order every
     // candidate, count and add of the block before it
     __syncthreads();
+    GBTOPK_TRACE_POINT(16, 0);
     if (ok && c.rhist[tid] != 0u) atomicAdd(row_hist(p, row) + tid, c.rhist[tid]);
     __syncthreads();
+    GBTOPK_TRACE_POINT(17, 0);
     if (tid == 0) {
         row_counts(p, row)[ch] = ok ? c.sel_count : 0xFFFFFFFFu;  // an unread chunk: the row falls back
         __threadfence();
+        GBTOPK_TRACE_POINT(18, 0);
         const uint32_t done = atomicAdd(info + 2, 1u);
         const bool is_last = done == static_cast<uint32_t>(nch - 1);
         if (is_last) __threadfence();  // acquire: every chunk's candidates, counts and histogram
@@ -2379,6 +2418,275 @@ __global__ void __launch_bounds__(128) small_kernel(const __grid_constant__ Para
     }
 }
 
+// Byte permute (PTX prmt, generic mode): selector nibble q picks byte q of
+// {b, a} for result byte i; a nibble with bit 3 set replicates that byte's
+// sign bit over the result byte.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Elem16::key of both halves of a word at once: a half whose magnitude is
+// zero loses its sign bit (-0 -> +0), then the negative halves are inverted
+// and the others get their top bit set.
+__device__ __forceinline__ uint32_t pair_keys(uint32_t w) {
+    const uint32_t nz = ((w & 0x7FFF7FFFu) + 0x7FFF7FFFu) & 0x80008000u;  // halves with a nonzero magnitude
+    const uint32_t v = w & (0x7FFF7FFFu | nz);
+    const uint32_t neg = prmt(v, 0u, 0xBB99u);  // 0xFFFF in each half whose sign bit is set
+    return v ^ (neg | 0x80008000u);
+}
+
+// Bit 15 (31) set iff the low (high) 16-bit half of a is >= the matching
+// half of T, for unsigned halves; Tlo = T & 0x7FFF7FFF.  The low 15 bits of
+// each half are compared by a subtraction that cannot borrow across halves
+// ((a | 0x8000) - (T & 0x7FFF) > 0), and the top bits decide where they
+// differ.  Other bits of the result are meaningless.
+__device__ __forceinline__ uint32_t pair_ge(uint32_t a, uint32_t T, uint32_t Tlo) {
+    const uint32_t x = (a | 0x80008000u) - Tlo;
+    return (a & ~T) | (~(a ^ T) & x);
+}
+
+// The digit holding the rem-th largest of the 256 counters h (shared
+// memory, one warp), counting from the top, after taking sub0 off bin 0:
+// the digit, the count of the bins above it and its own count.
+__device__ __forceinline__ void warp_digit(const uint32_t *h, uint32_t rem, uint32_t sub0, uint32_t &digit,
+                                           uint32_t &above, uint32_t &cnt) {
+    const uint32_t lane = lane_id();
+    // lane l owns bins 255 - 8 l down to 248 - 8 l
+    const uint4 lo = reinterpret_cast<const uint4 *>(h)[62 - 2 * lane];
+    const uint4 hi = reinterpret_cast<const uint4 *>(h)[63 - 2 * lane];
+    uint32_t c[8] = {hi.w, hi.z, hi.y, hi.x, lo.w, lo.z, lo.y, lo.x};
+    if (lane == 31) c[7] -= sub0;
+    uint32_t sum = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sum += c[j];
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= static_cast<uint32_t>(o)) incl += y;
+    }
+    const uint32_t excl = incl - sum;
+    const uint32_t owner = __ffs(__ballot_sync(0xffffffffu, excl < rem && rem <= incl)) - 1;
+    uint32_t d = 0, a = excl, nd = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        if (a + c[j] >= rem) {
+            d = 255u - 8u * lane - static_cast<uint32_t>(j);
+            nd = c[j];
+            break;
+        }
+        a += c[j];
+    }
+    digit = __shfl_sync(0xffffffffu, d, owner);
+    above = __shfl_sync(0xffffffffu, a, owner);
+    cnt = __shfl_sync(0xffffffffu, nd, owner);
+}
+
+// Small-row kernel for 16-bit rows (widths up to 64 * NW <= 2048, calls
+// without the sorted order): one warp per row, no block barrier.  Word w of
+// lane l holds the keys of columns 2 (l + 32 w) and 2 (l + 32 w) + 1, packed
+// (pair_keys), so a row takes NW registers; only the words that hold valid
+// columns are loaded or visited, and padding halves hold key 0 (the raw
+// value 0xFFFF), whose count is taken off digit 0 of each histogram.  The
+// k-th largest key t comes from two 8-bit radix rounds over a warp-private
+// shared histogram.  The output lists the keys > t and the first need =
+// k - #(keys > t) keys equal to t in column order (the last ones with the
+// largest-columns tie mode), word slice by word slice with two ballots per
+// word; when every key equal to t is taken, one packed compare per word
+// (pair_ge) decides.
+template <int DT, int NW>
+__global__ void __launch_bounds__(128, 7) small16_kernel(const __grid_constant__ Params p) {
+    static_assert(Elem<DT>::kBytes == 2, "16-bit rows");
+    using raw_t = typename Elem<DT>::raw_t;
+    const uint32_t lane = lane_id();
+    const uint32_t wid = threadIdx.x >> 5;
+    constexpr int kStageWords = 32 * NW + 8;  // a row of 64 NW columns and the 16-byte rounding on both sides
+    __shared__ __align__(16) uint32_t small_hist[4 * 256];  // one digit histogram per warp
+    __shared__ __align__(16) uint32_t small_stage[4][kStageWords];
+    __shared__ unsigned long long small_bar[4];
+    constexpr int kTraceBase = 0;
+    (void)kTraceBase;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    GBTOPK_TRACE_POINT(0, 0);
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+    if (row >= p.num_rows) return;  // whole warps
+    const int k = p.k;
+    int64_t n, col0;
+    row_window(p, row, n, col0);
+    const raw_t *xrow = static_cast<const raw_t *>(p.x) + row * p.row_stride + col0;
+    int32_t *out = p.out_idx + row * k;
+    if (n <= k) {  // short and empty rows: every valid column in order, then -1
+        for (int64_t j = lane; j < k; j += 32) out[j] = j < n ? static_cast<int32_t>(j) : -1;
+    } else {
+        const int nn = static_cast<int>(n);
+        const int nwv = (nn + 63) >> 6;  // words with a valid column (warp-uniform)
+        // the row is staged by one bulk copy (its bytes all in flight at once)
+        const Span sp = span_of<DT>(xrow, n);
+        unsigned long long *bar = &small_bar[wid];
+        uint32_t *stage = small_stage[wid];
+        if (lane == 0) {
+            mbar_init(bar);
+            bulk_load(stage, sp.a0, sp.bytes, bar);
+        }
+        uint32_t landed = lane == 0 ? (mbar_wait(bar, 0, p.wait_polls) ? 1u : 0u) : 0u;
+        landed = __shfl_sync(0xffffffffu, landed, 0);
+        uint32_t kw[NW];
+        if (landed) {
+            mbar_wait(bar, 0);  // completes at once: every lane sees the copied bytes
+            const int sh = (sp.off & 1) * 16;  // an odd first element straddles two words
+            const int wb = sp.off >> 1;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                uint32_t v = 0xFFFFFFFFu;
+                if (w < nwv) {
+                    const int q = wb + static_cast<int>(lane) + 32 * w;
+                    v = __funnelshift_r(stage[q], stage[q + 1], sh);
+                    if (w == nwv - 1) {  // the last visited word holds the row's end
+                        const int c = 2 * (static_cast<int>(lane) + 32 * w);
+                        if (c >= nn) v |= 0xFFFFu;
+                        if (c + 1 >= nn) v |= 0xFFFF0000u;
+                    }
+                }
+                kw[w] = pair_keys(v);
+            }
+        } else {  // the copy did not land in time: read the row from global memory
+            if (lane == 0) atomicOr(reinterpret_cast<uint32_t *>(p.ws), kStatusWaitTimeout);
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                uint32_t v = 0xFFFFFFFFu;
+                if (w < nwv) {
+                    const int c = 2 * (static_cast<int>(lane) + 32 * w);
+                    const uint32_t lo = c < nn ? ldg_raw(xrow + c) : 0xFFFFu;
+                    const uint32_t hi = c + 1 < nn ? ldg_raw(xrow + c + 1) : 0xFFFFu;
+                    v = lo | (hi << 16);
+                }
+                kw[w] = pair_keys(v);
+            }
+        }
+        GBTOPK_TRACE_POINT(1, 0);
+        const uint32_t pad = static_cast<uint32_t>(64 * nwv - nn);  // padding halves in the visited words
+        uint32_t *h = small_hist + (threadIdx.x >> 5) * 256;
+        // round 1: the top byte of the key
+        reinterpret_cast<uint4 *>(h)[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4 *>(h)[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
+        __syncwarp();
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            if (w < nwv) {
+                atomicAdd(&h[prmt(kw[w], 0u, 0x4441u)], 1u);
+                atomicAdd(&h[kw[w] >> 24], 1u);
+            }
+        }
+        __syncwarp();
+        uint32_t d1, above, cnt;
+        uint32_t rem = static_cast<uint32_t>(k);
+        warp_digit(h, rem, pad, d1, above, cnt);
+        rem -= above;
+        GBTOPK_TRACE_POINT(2, 0);
+        __syncwarp();
+        // round 2: the low byte, among the keys whose top byte is d1
+        reinterpret_cast<uint4 *>(h)[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4 *>(h)[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
+        __syncwarp();
+        const uint32_t pat = d1 * 0x01000100u;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            if (w < nwv) {
+                const uint32_t x = kw[w] ^ pat;
+                if ((x & 0xFF00u) == 0u) atomicAdd(&h[kw[w] & 0xFFu], 1u);
+                if (x < 0x01000000u) atomicAdd(&h[prmt(kw[w], 0u, 0x4442u)], 1u);
+            }
+        }
+        __syncwarp();
+        uint32_t d2, bin_n;
+        warp_digit(h, rem, d1 == 0u ? pad : 0u, d2, above, bin_n);
+        rem -= above;
+        GBTOPK_TRACE_POINT(3, 0);
+        const uint32_t t = (d1 << 8) | d2;
+        const uint32_t gt = static_cast<uint32_t>(k) - rem;  // keys > t
+        const uint32_t need = rem;                           // keys == t to take (1 <= need <= bin_n)
+        const uint32_t lt = lanemask_lt();
+        const uint32_t T = t | (t << 16);
+        uint32_t base = 0;
+        if (need == bin_n) {  // the output is every key >= t
+            const uint32_t Tlo = T & 0x7FFF7FFFu;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                if (w < nwv) {
+                    const uint32_t ge = pair_ge(kw[w], T, Tlo);
+                    const bool p0 = (ge & 0x8000u) != 0u, p1 = (ge & 0x80000000u) != 0u;
+                    const uint32_t b0 = __ballot_sync(0xffffffffu, p0), b1 = __ballot_sync(0xffffffffu, p1);
+                    const uint32_t s0 = base + __popc(b0 & lt) + __popc(b1 & lt);
+                    const int32_t c = 2 * (static_cast<int32_t>(lane) + 32 * w);
+                    if (p0) out[s0] = c;
+                    if (p1) out[s0 + (p0 ? 1u : 0u)] = c + 1;
+                    base += __popc(b0) + __popc(b1);
+                }
+            }
+        } else {  // some keys equal to t are left out: ties ranked in column order
+            const uint32_t skip = tie_mode(p.deterministic) == 2 ? bin_n - need : 0u;
+            uint32_t tie_base = 0;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                if (w < nwv) {
+                    const uint32_t a = kw[w];
+                    const uint32_t k0 = a & 0xFFFFu, k1 = a >> 16;
+                    const bool g0 = k0 > t, g1 = k1 > t, q0 = k0 == t, q1 = k1 == t;
+                    const uint32_t bg0 = __ballot_sync(0xffffffffu, g0), bg1 = __ballot_sync(0xffffffffu, g1);
+                    const uint32_t bq0 = __ballot_sync(0xffffffffu, q0), bq1 = __ballot_sync(0xffffffffu, q1);
+                    const uint32_t hs = base + __popc(bg0 & lt) + __popc(bg1 & lt);
+                    const uint32_t r0 = tie_base + __popc(bq0 & lt) + __popc(bq1 & lt) - skip;  // wraps when passed over
+                    const uint32_t r1 = r0 + (q0 ? 1u : 0u);
+                    const int32_t c = 2 * (static_cast<int32_t>(lane) + 32 * w);
+                    if (g0) out[hs] = c;
+                    if (g1) out[hs + (g0 ? 1u : 0u)] = c + 1;
+                    if (q0 && r0 < need) out[gt + r0] = c;
+                    if (q1 && r1 < need) out[gt + r1] = c + 1;
+                    base += __popc(bg0) + __popc(bg1);
+                    tie_base += __popc(bq0) + __popc(bq1);
+                }
+            }
+        }
+        if (!landed && lane == 0 && !mbar_wait(bar, 0))  // the stage must not be left with a copy in flight
+            atomicOr(reinterpret_cast<uint32_t *>(p.ws), kStatusCopyLost);
+        __syncwarp();
+    }
+    GBTOPK_TRACE_POINT(4, 0);
+    GBTOPK_TRACE_POINT(7, static_cast<unsigned long long>(n));
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (!p.page_table && !p.idx_offset && !p.out_val) return;
+    __syncwarp();  // the warp's index stores are visible to its lanes
+    const RowEpi ep = row_epilogue(p, row);
+#pragma unroll 1
+    for (int64_t j = lane; j < k; j += 32) {
+        const int32_t idx = out[j];
+        if (p.out_val)
+            static_cast<raw_t *>(p.out_val)[row * k + j] =
+                static_cast<raw_t>(idx >= 0 ? ldg_raw(xrow + idx) : Elem<DT>::kLowest);
+        if (p.page_table || p.idx_offset) {
+            if (p.out_raw) p.out_raw[row * k + j] = idx;
+            out[j] = out_index(p, ep, idx);
+        }
+    }
+}
+
+template <int DT, int NW>
+cudaError_t launch_small16(const Params &p, cudaStream_t stream) {
+    const unsigned grid = static_cast<unsigned>((p.num_rows + 3) / 4);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(128);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, small16_kernel<DT, NW>, p);
+}
+
 template <int DT, int NE>
 cudaError_t launch_small(const Params &p, cudaStream_t stream) {
     const unsigned grid = static_cast<unsigned>((p.num_rows + 3) / 4);
@@ -2453,9 +2761,15 @@ cudaError_t launch_dt(const Params &p0, cudaStream_t stream) {
         p.row0 = 0;
         p.rows = p0.num_rows;
         if (!sorted_output(p.deterministic) && p.width <= 32 * 64) {  // one warp per row
-            if (p.width <= 32 * 16) return launch_small<DT, 16>(p, stream);
-            if (p.width <= 32 * 32) return launch_small<DT, 32>(p, stream);
-            return launch_small<DT, 64>(p, stream);
+            if constexpr (Elem<DT>::kBytes == 2) {
+                if (p.width <= 64 * 8) return launch_small16<DT, 8>(p, stream);
+                if (p.width <= 64 * 16) return launch_small16<DT, 16>(p, stream);
+                return launch_small16<DT, 32>(p, stream);
+            } else {
+                if (p.width <= 32 * 16) return launch_small<DT, 16>(p, stream);
+                if (p.width <= 32 * 32) return launch_small<DT, 32>(p, stream);
+                return launch_small<DT, 64>(p, stream);
+            }
         }
         return launch_row_any<DT>(p, stream);
     }

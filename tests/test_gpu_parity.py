@@ -189,6 +189,29 @@ def test_small_rows_warp_path(dev, dtype, W):
         run_case(dev, c)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("W", [600, 2048])
+def test_small_rows_16bit_odd_offsets(dev, dtype, W):
+    """16-bit one-warp rows whose starts alternate between 4-byte aligned and
+    not (an odd row stride and an odd first element), so the warp reads some
+    rows as packed pairs and others element by element: ragged lengths, ties
+    at the k-th value taken in part, values on."""
+    g = torch.Generator().manual_seed(W + 31)
+    R = 24
+    x = torch.randn(R, W, generator=g)
+    x[::3] = torch.round(x[::3] * 8) / 8                           # ties at the k-th value
+    lens = torch.randint(0, W + 1, (R,), generator=g, dtype=torch.int32)
+    lens[0], lens[1], lens[2], lens[3] = W, W - 1, 513, 512
+
+    def offset_view(x, dev):
+        storage = torch.full((R, W + 3), POISON[x.dtype], dtype=x.dtype, device=dev)
+        storage[:, 1:W + 1] = x.to(dev)
+        return storage[:, 1:W + 1]
+    for k in (1, 100, 512):
+        c = workloads.VarlenCase("small16", x.to(dtype), lens, k)
+        run_case(dev, c, logits_view=offset_view)
+
+
 def test_small_rows_page_table(dev):
     c = workloads.page_table_case(rows=48, width=1500, row_stride=1531, page_size=16,
                                   pt_cols=128, top_k=256, deterministic=False, seed=5077)

@@ -31,20 +31,23 @@ def _child():
     dev = torch.device("cuda:0")
     g = torch.Generator().manual_seed(4242)
     cases = [
-        # (rows, width, k, deterministic): the stream path (more than 2048
-        # row-chunk slots), the fused chunk path, the one-block row path
-        (600, 70000, 2048, False),
-        (8, 100000, 2048, True),
-        (8, 100000, 1024, False),
-        (16, 12000, 1024, True),
+        # (rows, width, k, deterministic, dtype): the stream path (more than
+        # 2048 row-chunk slots), the fused chunk path, the one-block row path,
+        # the one-warp rows of 16-bit values
+        (600, 70000, 2048, False, torch.float32),
+        (8, 100000, 2048, True, torch.float32),
+        (8, 100000, 1024, False, torch.float32),
+        (16, 12000, 1024, True, torch.float32),
+        (64, 2048, 512, False, torch.float16),
     ]
-    for R, W, k, det in cases:
-        x = torch.round(torch.randn(R, W, generator=g) * 32) / 32
+    for R, W, k, det, dt in cases:
+        x = (torch.round(torch.randn(R, W, generator=g) * 32) / 32).to(dt)
         lens = torch.randint(k // 2, W + 1, (R,), generator=g, dtype=torch.int32)
-        plan = gb.gbtopk_plan_query(R, W, k, torch.float32)
+        lens[0] = W
+        plan = gb.gbtopk_plan_query(R, W, k, dt)
         ws = torch.zeros(plan["workspace_bytes"], dtype=torch.uint8, device=dev)
         out = torch.empty(R, k, dtype=torch.int32, device=dev)
-        val = torch.empty(R, k, dtype=torch.float32, device=dev)
+        val = torch.empty(R, k, dtype=dt, device=dev)
         st = gb.gbtopk_varlen(x.to(dev), lens.to(dev), k, None, 1, 1, out, val, det, ws)
         assert st == gb.OK
         torch.cuda.synchronize(dev)
@@ -52,13 +55,14 @@ def _child():
         assert flags & 1, f"{(R, W, k, det)}: no bounded wait gave up (flags {flags})"
         assert not flags & 2, f"{(R, W, k, det)}: a bulk copy never completed (flags {flags})"
         assert gb.gbtopk_device_status(ws) == 0  # read and cleared
-        rows = list(range(R)) if R <= 16 else [0, 1, 2, 299, 300, R - 2, R - 1]
+        rows = list(range(R)) if R <= 64 else [0, 1, 2, 299, 300, R - 2, R - 1]
         n = [min(int(lens[r]), W) for r in range(R)]
         ref = torch.full((R, k), -1, dtype=torch.int32)
         for r in rows:
             ref[r], _ = oracle.select_row(x[r], n[r], k, return_values=False)
         check_rows(x, n, k, out, ref, val, deterministic=det, rows=rows)
-        print(f"recovered: rows={R} width={W} k={k} sorted={det} plan={'fused' if plan['fused'] else ('stream' if plan['split'] else 'row')}")
+        kind = "fused" if plan["fused"] else ("stream" if plan["split"] else ("warp" if W <= 2048 and not det else "row"))
+        print(f"recovered: rows={R} width={W} k={k} sorted={det} plan={kind}")
     print("child: ok")
 
 
@@ -69,7 +73,7 @@ def test_waits_that_give_up_leave_outputs_exact():
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "child"], env=env,
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 0 and "child: ok" in r.stdout, r.stdout[-3000:] + r.stderr[-3000:]
-    for kind in ("stream", "fused", "row"):
+    for kind in ("stream", "fused", "row", "warp"):
         assert f"plan={kind}" in r.stdout, f"the {kind} path was not exercised"
 
 
