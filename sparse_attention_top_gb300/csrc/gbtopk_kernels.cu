@@ -2484,18 +2484,105 @@ __device__ __forceinline__ void warp_digit(const uint32_t *h, uint32_t rem, uint
     cnt = __shfl_sync(0xffffffffu, nd, owner);
 }
 
+// The selection of one 16-bit row of nn > k valid columns by one warp
+// (small16_kernel): word w of lane l holds the keys of columns
+// 2 (l + 32 w) and 2 (l + 32 w) + 1, packed (pair_keys), and key_word(w)
+// returns it for the words w < nwv that hold valid columns; padding halves
+// hold key 0 (the raw value 0xFFFF), whose count is taken off digit 0 of
+// each histogram.  The k-th largest key t comes from two 8-bit radix rounds
+// over the warp's shared histogram h.  The output lists the keys > t and
+// the first need = k - #(keys > t) keys equal to t in column order (the
+// last ones with the largest-columns tie mode), word by word with two
+// ballots per word; when every key equal to t is taken, one packed compare
+// per word (pair_ge) decides.
+template <class KeyWord>
+__device__ __forceinline__ void small16_select(const Params &p, int nn, int nwv, uint32_t *h, int32_t *out,
+                                               const KeyWord &key_word) {
+    const uint32_t lane = lane_id();
+    const int k = p.k;
+    const uint32_t pad = static_cast<uint32_t>(64 * nwv - nn);  // padding halves in the visited words
+    // round 1: the top byte of the key
+    reinterpret_cast<uint4 *>(h)[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4 *>(h)[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+#pragma unroll 4
+    for (int w = 0; w < nwv; ++w) {
+        const uint32_t kw = key_word(w);
+        atomicAdd(&h[prmt(kw, 0u, 0x4441u)], 1u);
+        atomicAdd(&h[kw >> 24], 1u);
+    }
+    __syncwarp();
+    uint32_t d1, above, cnt;
+    uint32_t rem = static_cast<uint32_t>(k);
+    warp_digit(h, rem, pad, d1, above, cnt);
+    rem -= above;
+    __syncwarp();
+    // round 2: the low byte, among the keys whose top byte is d1
+    reinterpret_cast<uint4 *>(h)[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4 *>(h)[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+    const uint32_t pat = d1 * 0x01000100u;
+#pragma unroll 4
+    for (int w = 0; w < nwv; ++w) {
+        const uint32_t kw = key_word(w);
+        const uint32_t x = kw ^ pat;
+        if ((x & 0xFF00u) == 0u) atomicAdd(&h[kw & 0xFFu], 1u);
+        if (x < 0x01000000u) atomicAdd(&h[prmt(kw, 0u, 0x4442u)], 1u);
+    }
+    __syncwarp();
+    uint32_t d2, bin_n;
+    warp_digit(h, rem, d1 == 0u ? pad : 0u, d2, above, bin_n);
+    rem -= above;
+    const uint32_t t = (d1 << 8) | d2;
+    const uint32_t gt = static_cast<uint32_t>(k) - rem;  // keys > t
+    const uint32_t need = rem;                           // keys == t to take (1 <= need <= bin_n)
+    const uint32_t lt = lanemask_lt();
+    const uint32_t T = t | (t << 16);
+    uint32_t base = 0;
+    if (need == bin_n) {  // the output is every key >= t
+        const uint32_t Tlo = T & 0x7FFF7FFFu;
+#pragma unroll 4
+        for (int w = 0; w < nwv; ++w) {
+            const uint32_t ge = pair_ge(key_word(w), T, Tlo);
+            const bool p0 = (ge & 0x8000u) != 0u, p1 = (ge & 0x80000000u) != 0u;
+            const uint32_t b0 = __ballot_sync(0xffffffffu, p0), b1 = __ballot_sync(0xffffffffu, p1);
+            const uint32_t s0 = base + __popc(b0 & lt) + __popc(b1 & lt);
+            const int32_t c = 2 * (static_cast<int32_t>(lane) + 32 * w);
+            if (p0) out[s0] = c;
+            if (p1) out[s0 + (p0 ? 1u : 0u)] = c + 1;
+            base += __popc(b0) + __popc(b1);
+        }
+    } else {  // some keys equal to t are left out: ties ranked in column order
+        const uint32_t skip = tie_mode(p.deterministic) == 2 ? bin_n - need : 0u;
+        uint32_t tie_base = 0;
+#pragma unroll 2
+        for (int w = 0; w < nwv; ++w) {
+            const uint32_t a = key_word(w);
+            const uint32_t k0 = a & 0xFFFFu, k1 = a >> 16;
+            const bool g0 = k0 > t, g1 = k1 > t, q0 = k0 == t, q1 = k1 == t;
+            const uint32_t bg0 = __ballot_sync(0xffffffffu, g0), bg1 = __ballot_sync(0xffffffffu, g1);
+            const uint32_t bq0 = __ballot_sync(0xffffffffu, q0), bq1 = __ballot_sync(0xffffffffu, q1);
+            const uint32_t hs = base + __popc(bg0 & lt) + __popc(bg1 & lt);
+            const uint32_t r0 = tie_base + __popc(bq0 & lt) + __popc(bq1 & lt) - skip;  // wraps when passed over
+            const uint32_t r1 = r0 + (q0 ? 1u : 0u);
+            const int32_t c = 2 * (static_cast<int32_t>(lane) + 32 * w);
+            if (g0) out[hs] = c;
+            if (g1) out[hs + (g0 ? 1u : 0u)] = c + 1;
+            if (q0 && r0 < need) out[gt + r0] = c;
+            if (q1 && r1 < need) out[gt + r1] = c + 1;
+            base += __popc(bg0) + __popc(bg1);
+            tie_base += __popc(bq0) + __popc(bq1);
+        }
+    }
+}
+
 // Small-row kernel for 16-bit rows (widths up to 64 * NW <= 2048, calls
-// without the sorted order): one warp per row, no block barrier.  Word w of
-// lane l holds the keys of columns 2 (l + 32 w) and 2 (l + 32 w) + 1, packed
-// (pair_keys), so a row takes NW registers; only the words that hold valid
-// columns are loaded or visited, and padding halves hold key 0 (the raw
-// value 0xFFFF), whose count is taken off digit 0 of each histogram.  The
-// k-th largest key t comes from two 8-bit radix rounds over a warp-private
-// shared histogram.  The output lists the keys > t and the first need =
-// k - #(keys > t) keys equal to t in column order (the last ones with the
-// largest-columns tie mode), word slice by word slice with two ballots per
-// word; when every key equal to t is taken, one packed compare per word
-// (pair_ge) decides.
+// without the sorted order): one warp per row, no block barrier.  A row
+// longer than k is staged by one bulk copy (its bytes all in flight at
+// once), turned into packed keys in place and selected by small16_select;
+// if the copy does not land within the first bounded wait, the keys are
+// read from global memory instead (status bit 0), and the warp waits again
+// (bounded) for the copy before it leaves.
 template <int DT, int NW>
 __global__ void __launch_bounds__(128, 7) small16_kernel(const __grid_constant__ Params p) {
     static_assert(Elem<DT>::kBytes == 2, "16-bit rows");
@@ -2510,7 +2597,7 @@ __global__ void __launch_bounds__(128, 7) small16_kernel(const __grid_constant__
     (void)kTraceBase;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     GBTOPK_TRACE_POINT(0, 0);
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + wid;
     if (row >= p.num_rows) return;  // whole warps
     const int k = p.k;
     int64_t n, col0;
@@ -2522,136 +2609,46 @@ __global__ void __launch_bounds__(128, 7) small16_kernel(const __grid_constant__
     } else {
         const int nn = static_cast<int>(n);
         const int nwv = (nn + 63) >> 6;  // words with a valid column (warp-uniform)
-        // the row is staged by one bulk copy (its bytes all in flight at once)
         const Span sp = span_of<DT>(xrow, n);
         unsigned long long *bar = &small_bar[wid];
         uint32_t *stage = small_stage[wid];
+        uint32_t *h = small_hist + wid * 256;
         if (lane == 0) {
             mbar_init(bar);
             bulk_load(stage, sp.a0, sp.bytes, bar);
         }
         uint32_t landed = lane == 0 ? (mbar_wait(bar, 0, p.wait_polls) ? 1u : 0u) : 0u;
         landed = __shfl_sync(0xffffffffu, landed, 0);
-        uint32_t kw[NW];
         if (landed) {
             mbar_wait(bar, 0);  // completes at once: every lane sees the copied bytes
-            const int sh = (sp.off & 1) * 16;  // an odd first element straddles two words
+            // the packed keys, in place: word w of lane l to stage[l + 32 w]
+            // (an odd first element straddles two copied words)
+            const int sh = (sp.off & 1) * 16;
             const int wb = sp.off >> 1;
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                uint32_t v = 0xFFFFFFFFu;
-                if (w < nwv) {
-                    const int q = wb + static_cast<int>(lane) + 32 * w;
-                    v = __funnelshift_r(stage[q], stage[q + 1], sh);
-                    if (w == nwv - 1) {  // the last visited word holds the row's end
-                        const int c = 2 * (static_cast<int>(lane) + 32 * w);
-                        if (c >= nn) v |= 0xFFFFu;
-                        if (c + 1 >= nn) v |= 0xFFFF0000u;
-                    }
-                }
-                kw[w] = pair_keys(v);
+            for (int w = 0; w < nwv; ++w) {
+                const int q = wb + static_cast<int>(lane) + 32 * w;
+                uint32_t v = __funnelshift_r(stage[q], stage[q + 1], sh);
+                const int c = 2 * (static_cast<int>(lane) + 32 * w);
+                if (c >= nn) v |= 0xFFFFu;
+                if (c + 1 >= nn) v |= 0xFFFF0000u;
+                __syncwarp();  // every lane has read before any lane writes
+                stage[lane + 32 * w] = pair_keys(v);
             }
+            __syncwarp();
+            GBTOPK_TRACE_POINT(1, 0);
+            small16_select(p, nn, nwv, h, out, [&](int w) { return stage[lane + 32 * w]; });
         } else {  // the copy did not land in time: read the row from global memory
             if (lane == 0) atomicOr(reinterpret_cast<uint32_t *>(p.ws), kStatusWaitTimeout);
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                uint32_t v = 0xFFFFFFFFu;
-                if (w < nwv) {
-                    const int c = 2 * (static_cast<int>(lane) + 32 * w);
-                    const uint32_t lo = c < nn ? ldg_raw(xrow + c) : 0xFFFFu;
-                    const uint32_t hi = c + 1 < nn ? ldg_raw(xrow + c + 1) : 0xFFFFu;
-                    v = lo | (hi << 16);
-                }
-                kw[w] = pair_keys(v);
-            }
+            small16_select(p, nn, nwv, h, out, [&](int w) {
+                const int c = 2 * (static_cast<int>(lane) + 32 * w);
+                const uint32_t lo = c < nn ? ldg_raw(xrow + c) : 0xFFFFu;
+                const uint32_t hi = c + 1 < nn ? ldg_raw(xrow + c + 1) : 0xFFFFu;
+                return pair_keys(lo | (hi << 16));
+            });
+            if (lane == 0 && !mbar_wait(bar, 0))  // the stage must not be left with a copy in flight
+                atomicOr(reinterpret_cast<uint32_t *>(p.ws), kStatusCopyLost);
+            __syncwarp();
         }
-        GBTOPK_TRACE_POINT(1, 0);
-        const uint32_t pad = static_cast<uint32_t>(64 * nwv - nn);  // padding halves in the visited words
-        uint32_t *h = small_hist + (threadIdx.x >> 5) * 256;
-        // round 1: the top byte of the key
-        reinterpret_cast<uint4 *>(h)[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
-        reinterpret_cast<uint4 *>(h)[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
-        __syncwarp();
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            if (w < nwv) {
-                atomicAdd(&h[prmt(kw[w], 0u, 0x4441u)], 1u);
-                atomicAdd(&h[kw[w] >> 24], 1u);
-            }
-        }
-        __syncwarp();
-        uint32_t d1, above, cnt;
-        uint32_t rem = static_cast<uint32_t>(k);
-        warp_digit(h, rem, pad, d1, above, cnt);
-        rem -= above;
-        GBTOPK_TRACE_POINT(2, 0);
-        __syncwarp();
-        // round 2: the low byte, among the keys whose top byte is d1
-        reinterpret_cast<uint4 *>(h)[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
-        reinterpret_cast<uint4 *>(h)[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
-        __syncwarp();
-        const uint32_t pat = d1 * 0x01000100u;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            if (w < nwv) {
-                const uint32_t x = kw[w] ^ pat;
-                if ((x & 0xFF00u) == 0u) atomicAdd(&h[kw[w] & 0xFFu], 1u);
-                if (x < 0x01000000u) atomicAdd(&h[prmt(kw[w], 0u, 0x4442u)], 1u);
-            }
-        }
-        __syncwarp();
-        uint32_t d2, bin_n;
-        warp_digit(h, rem, d1 == 0u ? pad : 0u, d2, above, bin_n);
-        rem -= above;
-        GBTOPK_TRACE_POINT(3, 0);
-        const uint32_t t = (d1 << 8) | d2;
-        const uint32_t gt = static_cast<uint32_t>(k) - rem;  // keys > t
-        const uint32_t need = rem;                           // keys == t to take (1 <= need <= bin_n)
-        const uint32_t lt = lanemask_lt();
-        const uint32_t T = t | (t << 16);
-        uint32_t base = 0;
-        if (need == bin_n) {  // the output is every key >= t
-            const uint32_t Tlo = T & 0x7FFF7FFFu;
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                if (w < nwv) {
-                    const uint32_t ge = pair_ge(kw[w], T, Tlo);
-                    const bool p0 = (ge & 0x8000u) != 0u, p1 = (ge & 0x80000000u) != 0u;
-                    const uint32_t b0 = __ballot_sync(0xffffffffu, p0), b1 = __ballot_sync(0xffffffffu, p1);
-                    const uint32_t s0 = base + __popc(b0 & lt) + __popc(b1 & lt);
-                    const int32_t c = 2 * (static_cast<int32_t>(lane) + 32 * w);
-                    if (p0) out[s0] = c;
-                    if (p1) out[s0 + (p0 ? 1u : 0u)] = c + 1;
-                    base += __popc(b0) + __popc(b1);
-                }
-            }
-        } else {  // some keys equal to t are left out: ties ranked in column order
-            const uint32_t skip = tie_mode(p.deterministic) == 2 ? bin_n - need : 0u;
-            uint32_t tie_base = 0;
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                if (w < nwv) {
-                    const uint32_t a = kw[w];
-                    const uint32_t k0 = a & 0xFFFFu, k1 = a >> 16;
-                    const bool g0 = k0 > t, g1 = k1 > t, q0 = k0 == t, q1 = k1 == t;
-                    const uint32_t bg0 = __ballot_sync(0xffffffffu, g0), bg1 = __ballot_sync(0xffffffffu, g1);
-                    const uint32_t bq0 = __ballot_sync(0xffffffffu, q0), bq1 = __ballot_sync(0xffffffffu, q1);
-                    const uint32_t hs = base + __popc(bg0 & lt) + __popc(bg1 & lt);
-                    const uint32_t r0 = tie_base + __popc(bq0 & lt) + __popc(bq1 & lt) - skip;  // wraps when passed over
-                    const uint32_t r1 = r0 + (q0 ? 1u : 0u);
-                    const int32_t c = 2 * (static_cast<int32_t>(lane) + 32 * w);
-                    if (g0) out[hs] = c;
-                    if (g1) out[hs + (g0 ? 1u : 0u)] = c + 1;
-                    if (q0 && r0 < need) out[gt + r0] = c;
-                    if (q1 && r1 < need) out[gt + r1] = c + 1;
-                    base += __popc(bg0) + __popc(bg1);
-                    tie_base += __popc(bq0) + __popc(bq1);
-                }
-            }
-        }
-        if (!landed && lane == 0 && !mbar_wait(bar, 0))  // the stage must not be left with a copy in flight
-            atomicOr(reinterpret_cast<uint32_t *>(p.ws), kStatusCopyLost);
-        __syncwarp();
     }
     GBTOPK_TRACE_POINT(4, 0);
     GBTOPK_TRACE_POINT(7, static_cast<unsigned long long>(n));
