@@ -30,6 +30,7 @@
 // the guess.  Ranking uses order-preserving integer keys (signed zeros
 // equal; +-inf and denormals exact), so no float compare depends on
 // flush-to-zero.
+#include <cstddef>
 #include <cstdint>
 #include <map>
 #include <mutex>
@@ -134,7 +135,7 @@ struct Ctrl {
     uint32_t abort_flag;     // stream kernel: a bounded wait gave up, stop streaming
     uint32_t pad[2];
     uint32_t scan[72];
-    uint32_t rhist[256];     // radix-select digit histogram
+    alignas(16) uint32_t rhist[256];  // radix-select digit histogram (read with vector loads)
     uint32_t key_min;
     unsigned long long full[kStages];   // stream ring: stage filled (bulk copy landed)
     unsigned long long empty[kStages];  // stream ring: stage read by every consumer warp
@@ -143,6 +144,7 @@ struct Ctrl {
     unsigned long long scombo[2][kStages];
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
+static_assert(offsetof(Ctrl, rhist) % 16 == 0, "vector loads of the digit histogram");
 
 // ---------------------------------------------------------------- small helpers
 
@@ -877,12 +879,19 @@ __device__ __forceinline__ void warp_find_two_bins(const uint32_t *hist, uint32_
     constexpr int PER = NB / 32;
     if (threadIdx.x >= 32) return;
     const uint32_t lane = lane_id();
+    static_assert(PER % 4 == 0, "vector loads");
     uint32_t cnt[PER], s = 0;
+    const uint4 *h4 = reinterpret_cast<const uint4 *>(hist + NB - PER * (static_cast<int>(lane) + 1));
 #pragma unroll
-    for (int j = 0; j < PER; ++j) {
-        cnt[j] = hist[NB - 1 - PER * static_cast<int>(lane) - j];
-        s += cnt[j];
+    for (int q = 0; q < PER / 4; ++q) {
+        const uint4 v = h4[q];
+        cnt[PER - 1 - 4 * q] = v.x;
+        cnt[PER - 2 - 4 * q] = v.y;
+        cnt[PER - 3 - 4 * q] = v.z;
+        cnt[PER - 4 - 4 * q] = v.w;
     }
+#pragma unroll
+    for (int j = 0; j < PER; ++j) s += cnt[j];
     uint32_t incl = s;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -1652,12 +1661,13 @@ __device__ __forceinline__ void coarse_select(const uint32_t *hist, uint32_t r, 
     static_assert(kCoarseBins == 256, "eight bins per lane");
     if (threadIdx.x >= 32) return;
     const uint32_t lane = lane_id();
-    uint32_t cnts[8], s = 0;
+    // bins 255 - 8 lane - j, from the top (two vector loads; hist is 16-byte aligned)
+    const uint4 lo = reinterpret_cast<const uint4 *>(hist)[62 - 2 * lane];
+    const uint4 hi = reinterpret_cast<const uint4 *>(hist)[63 - 2 * lane];
+    const uint32_t cnts[8] = {hi.w, hi.z, hi.y, hi.x, lo.w, lo.z, lo.y, lo.x};
+    uint32_t s = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {  // bins 255 - 8 lane - j, from the top
-        cnts[j] = hist[255 - 8 * lane - j];
-        s += cnts[j];
-    }
+    for (int j = 0; j < 8; ++j) s += cnts[j];
     uint32_t incl = s;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
