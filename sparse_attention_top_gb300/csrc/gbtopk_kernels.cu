@@ -2176,9 +2176,10 @@ __global__ void __launch_bounds__(kThreads, 3) chunk_kernel(const __grid_constan
     constexpr int kTraceBase = kTraceChunk;
     (void)kTraceBase;
     GBTOPK_TRACE_POINT(0, 0);
-    const int64_t cpr = p.plan.chunks_per_row;
-    const int64_t row = p.row0 + static_cast<int64_t>(blockIdx.x) / cpr;
-    const int64_t ch = static_cast<int64_t>(blockIdx.x) % cpr;
+    // chunk-major slots (block b: chunk b / rows of row b % rows), so the
+    // blocks of every row's first chunks, which always hold data, launch first
+    const int64_t row = p.row0 + static_cast<int64_t>(blockIdx.x) % p.rows;
+    const int64_t ch = static_cast<int64_t>(blockIdx.x) / p.rows;
     int64_t n, col0;
     row_window(p, row, n, col0);
     const int64_t nch = split_chunks(p, n);
