@@ -630,7 +630,8 @@ __device__ __forceinline__ unsigned long long sort_composite(uint2 v) {
 // (det_scratch_bytes(sel_cap) bytes in all).  All NT threads call it.
 template <int DT, int NT, bool Compact>
 __device__ void emit_sorted_impl(const Params &p, int64_t row, const uint2 *sel, int m, uint8_t *scratch,
-                                 Ctrl &c) {
+                                 Ctrl &c, int64_t trace_idx) {
+    (void)trace_idx;  // the trace row of this block (GBTOPK_TRACE builds; < 0: none)
     uint32_t *bins = reinterpret_cast<uint32_t *>(scratch);
     unsigned long long *comp = reinterpret_cast<unsigned long long *>(scratch + kBins * 4);
     uint16_t *pos = reinterpret_cast<uint16_t *>(
@@ -650,6 +651,7 @@ __device__ void emit_sorted_impl(const Params &p, int64_t row, const uint2 *sel,
         kmax = key > kmax ? key : kmax;
     }
     block_minmax(kmin, kmax, c);
+    if (tid == 0 && trace_idx >= 0) GBTOPK_TRACE_SET(trace_idx, 22, -1);
     if (NT == kFinalThreads && tid == 0) GBTOPK_TRACE_SET(kTraceFinal + blockIdx.x, 3, -1);
     kmin = c.key_min;
     const int bits = 32 - __clz(c.key_max - kmin);
@@ -657,8 +659,10 @@ __device__ void emit_sorted_impl(const Params &p, int64_t row, const uint2 *sel,
     for (int i = tid; i < m; i += NT)
         atomicAdd(&bins[(Elem<DT>::key(sel[i].x) - kmin) >> shift], 1u);
     __syncthreads();
+    if (tid == 0 && trace_idx >= 0) GBTOPK_TRACE_SET(trace_idx, 23, -1);
     // bins[b] = pairs in the bins above b
     scan_from_top<NT, kBins>(bins, c, [&](uint32_t b, uint32_t above, uint32_t) { bins[b] = above; });
+    if (tid == 0 && trace_idx >= 0) GBTOPK_TRACE_SET(trace_idx, 24, -1);
     if (NT == kFinalThreads && tid == 0) GBTOPK_TRACE_SET(kTraceFinal + blockIdx.x, 4, -1);
     for (int i = tid; i < m; i += NT) {
         const uint2 v = sel[i];
@@ -667,6 +671,7 @@ __device__ void emit_sorted_impl(const Params &p, int64_t row, const uint2 *sel,
         if constexpr (!Compact) comp[at] = sort_composite<DT>(v);
     }
     __syncthreads();
+    if (tid == 0 && trace_idx >= 0) GBTOPK_TRACE_SET(trace_idx, 25, -1);
     if (NT == kFinalThreads && tid == 0) GBTOPK_TRACE_SET(kTraceFinal + blockIdx.x, 5, -1);
     // bins[b] now ends b's segment, which starts where b + 1's ends
     if constexpr (Compact) {
@@ -694,6 +699,7 @@ __device__ void emit_sorted_impl(const Params &p, int64_t row, const uint2 *sel,
             inv[lo + before] = pos[j];
         }
         __syncthreads();
+        if (tid == 0 && trace_idx >= 0) GBTOPK_TRACE_SET(trace_idx, 26, -1);
         if (NT == kFinalThreads && tid == 0) GBTOPK_TRACE_SET(kTraceFinal + blockIdx.x, 8, -1);
 #pragma unroll 4
         for (int j = tid; j < m; j += NT) {
@@ -703,13 +709,15 @@ __device__ void emit_sorted_impl(const Params &p, int64_t row, const uint2 *sel,
     }
     for (int j = m + tid; j < p.k; j += NT) put_mapped<DT>(p, row, j, -1, -1, 0u);
     __syncthreads();
+    if (tid == 0 && trace_idx >= 0) GBTOPK_TRACE_SET(trace_idx, 27, -1);
 }
 
 // The sorted output with the segment form the plan's scratch was sized for.
 template <int DT, int NT>
-__device__ void emit_sorted(const Params &p, int64_t row, const uint2 *sel, int m, uint8_t *scratch, Ctrl &c) {
-    if (p.plan.sel_cap <= kPairSortMax) emit_sorted_impl<DT, NT, false>(p, row, sel, m, scratch, c);
-    else emit_sorted_impl<DT, NT, true>(p, row, sel, m, scratch, c);
+__device__ void emit_sorted(const Params &p, int64_t row, const uint2 *sel, int m, uint8_t *scratch, Ctrl &c,
+                            int64_t trace_idx = -1) {
+    if (p.plan.sel_cap <= kPairSortMax) emit_sorted_impl<DT, NT, false>(p, row, sel, m, scratch, c, trace_idx);
+    else emit_sorted_impl<DT, NT, true>(p, row, sel, m, scratch, c, trace_idx);
 }
 
 // ---------------------------------------------------------------- bulk staging
@@ -2102,7 +2110,7 @@ __device__ void finalize_row(const Params &p, int64_t row, int64_t n, int64_t co
     }
     if (sorted && scratch_ok) {
         __syncthreads();
-        emit_sorted<DT, NT>(p, row, fr.sel, k, fr.scratch, c);
+        emit_sorted<DT, NT>(p, row, fr.sel, k, fr.scratch, c, trace_idx);
     } else {
         emit<DT>(p, row, fr.sel, k);  // the selected set, unordered if the scratch was unusable
     }
