@@ -57,7 +57,7 @@ int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *p
     const size_t sel_bytes = static_cast<size_t>(sel_cap) * 8;
     size_t hist = sel_bytes > guess ? sel_bytes : guess;
     if (hist < static_cast<size_t>(kBins) * 4) hist = static_cast<size_t>(kBins) * 4;
-    if (width <= 2 * chunk) {
+    if (width * es <= kDirectBytes) {
         pl.split = 0;
         pl.direct_max = static_cast<int32_t>(width);
         pl.chunks_per_row = 1;
@@ -90,7 +90,7 @@ int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *p
         pl.split = 1;
         pl.direct_max = top_k;
         pl.chunks_per_row = static_cast<int32_t>((width + chunk - 1) / chunk);
-        if (pl.chunks_per_row > kFinalThreads) return GBTOPK_EUNSUPPORTED;
+        if (pl.chunks_per_row > kThreads) return GBTOPK_EUNSUPPORTED;  // the same width limit as the fused path
         pl.block_rows = num_rows < kMaxBlockRows ? num_rows : kMaxBlockRows;
         // control block, the row table of one launch, the ring (a small
         // batch's stream block still fits beside a row-kernel block)

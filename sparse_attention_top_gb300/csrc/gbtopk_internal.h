@@ -20,9 +20,10 @@ constexpr int kGuessBins = 512;        // bins of each round of the sample's thr
 constexpr int kRankMax = 256;          // boundary-bin size resolved by rank counting
 constexpr int kRankAllMax = 64;        // the same in the finalize (a block radix select above)
 constexpr size_t kCtrlBytes = 2048;    // per-block control block (counters, scan, digit histogram)
-constexpr int kChunkBytes = 32768;     // bytes per stream chunk (one bulk copy)
-constexpr int kStages = 6;             // bulk-copy ring depth of the stream kernel
-constexpr int kGroupWarps = 8;         // consumer warps that share one chunk
+constexpr int kChunkBytes = 65536;     // bytes per stream chunk (one bulk copy)
+constexpr int kStages = 3;             // bulk-copy ring depth of the stream kernel
+constexpr int kGroupWarps = 16;        // consumer warps that share one chunk
+constexpr int kDirectBytes = 65536;    // rows of at most this many bytes: one block per row
 constexpr int kStageBytes = kChunkBytes + 32;  // a chunk plus its 16-byte alignment slack
 constexpr int kStreamThreads = 544;    // stream kernel: 1 producer warp + 16 consumer warps
 constexpr int kFinalHistBytes = 16384; // finalize histogram / selection buffer

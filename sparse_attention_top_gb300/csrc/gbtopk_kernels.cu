@@ -9,7 +9,7 @@
 //   * n == 0 or n <= k -> every valid column, then -1 (short path);
 //   * widths up to 2048 without the sorted order: one warp per row
 //     (small_kernel, a warp-private radix select on keys in registers);
-//   * widths up to two 32 KB chunks: one block per row (row_kernel): the
+//   * rows of up to 64 KB: one block per row (row_kernel): the
 //     row is staged in shared memory by one bulk copy, a threshold is
 //     guessed from a strided sample, the elements at or above it are kept
 //     and selected exactly in shared memory;
@@ -1358,12 +1358,15 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
 // rows, block b taking chunks b, b + G, b + 2G, ... of the dense row-major
 // chunk list.  Warp 0 is the producer: it maps chunks to rows and issues
 // their bulk copies into a ring of kStages shared-memory stages ("full"
-// barriers carry the byte counts).  The other warps are consumers: each
-// loads its slice of a stage into registers, releases the stage ("empty"
-// barrier), keeps the elements at or above the row's guess and appends them
-// to that chunk's fixed segment in the workspace (one shared atomic per warp
-// reserves the slots); the last warp to finish a chunk stores its count.
-// There is no block-wide barrier in the steady state.
+// barriers carry the byte counts).  The other warps are consumers, one group
+// per chunk: each loads its slice of the stage into registers, keeps the
+// elements at or above the row's guess and appends them to that chunk's
+// fixed segment in the workspace (one shared atomic per warp reserves the
+// slots; the values are read back from the stage), then releases the stage
+// ("empty" barrier); the last warp to finish a chunk stores its count.
+// Three 64 KB stages per SM measured faster than six of 32 KB or four of
+// 48 KB (fewer, larger copies).  There is no block-wide barrier in the
+// steady state.
 struct StageMeta {
     int64_t c0;       // first column of the chunk
     int32_t row;      // row index within this launch
@@ -1397,7 +1400,7 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
     constexpr int es = Elem<DT>::kBytes;
     constexpr int EPV = 16 / es;
     constexpr int NCW = kStreamThreads / 32 - 1;  // consumer warps
-    constexpr int kGroups = NCW / kGroupWarps;      // consumer groups take alternate chunks
+    constexpr int kGroups = NCW / kGroupWarps;      // consumer groups take chunks in turn
     constexpr int VPL = (kChunkBytes + 16) / 16 / (kGroupWarps * 32) + 1;
     static_assert(kStages % kGroups == 0, "each group cycles its own stages");
     extern __shared__ __align__(128) uint8_t smem[];

@@ -149,11 +149,11 @@ def test_plan_totality_and_consistency():
         dt = rnd.choice(dts)
         p = gb.gbtopk_plan_query(R, W, k, dt)
         es = 4 if dt == torch.float32 else 2
-        # two-kernel (fused) split path up to top_k 2048, 64 KB chunks; the
-        # three-kernel path above it, 32 KB chunks
+        # two-kernel (fused) split path up to top_k 2048 and the three-kernel
+        # path above it, both with 64 KB chunks
         fused_slots = R * -(-W * es // 65536)
         assert p["fused"] == int(bool(p["split"]) and k <= 2048 and fused_slots <= 2048)
-        assert p["chunk"] * es == (65536 if p["fused"] else 32768)
+        assert p["chunk"] * es == 65536
         for key in ("row_smem", "row_smem_sorted", "stream_smem", "final_smem", "fused_smem"):
             assert p[key] <= 227 * 1024
         assert p["row_smem_sorted"] >= p["row_smem"]
@@ -164,8 +164,8 @@ def test_plan_totality_and_consistency():
         elif p["split"] and R <= 128:
             assert p["row_smem"] + p["stream_smem"] + 2048 <= 228 * 1024
         if p["split"]:
-            assert W > 2 * 32768 // es and p["direct_max"] == k
-            assert p["chunk"] * p["chunks_per_row"] >= W
+            assert W > 65536 // es and p["direct_max"] == k
+            assert p["chunk"] * p["chunks_per_row"] >= W and p["chunks_per_row"] <= 256
             assert p["row_candidates"] >= k and p["ws_row_bytes"] >= 8 * p["row_candidates"]
         else:
             assert p["direct_max"] == W and p["chunks_per_row"] == 1 and p["ws_row_bytes"] == 0

@@ -569,6 +569,27 @@ def test_more_rows_than_one_launch(dev):
     run_case(dev, c, rows=[0, 1, 1000, 2046, 2047, 2048, 2049, 2099], poison=False, values=False)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_stream_chunk_boundaries(dev, dtype):
+    """Batches past the two-kernel path's slot limit take the persistent ring
+    of 64 KB chunks: lengths one below, at and one past each chunk boundary,
+    at the width, and around k, on sampled rows."""
+    es = 4 if dtype == torch.float32 else 2
+    CH = 65536 // es
+    R, W, k = 420, 5 * CH + 100, 2048
+    plan = gb.gbtopk_plan_query(R, W, k, dtype)
+    assert plan["split"] == 1 and plan["fused"] == 0 and plan["chunk"] == CH
+    g = torch.Generator().manual_seed(8300 + es)
+    x = torch.randn(R, W, generator=g).to(dtype)
+    lens = torch.randint(k + 1, W + 1, (R,), generator=g, dtype=torch.int32)
+    picks = [CH * j + d for j in range(1, 6) for d in (-1, 0, 1)] + [W, W - 1, k + 1, k, 300]
+    rows = [7 * i + 3 for i in range(len(picks))]
+    for r, n in zip(rows, picks):
+        lens[r] = n
+    c = workloads.VarlenCase("stream_bounds", x, lens, k)
+    run_case(dev, c, rows=rows + [0, R - 1], poison=False)
+
+
 @pytest.mark.parametrize("k", [1, 2048])
 def test_widest_rows(dev, k):
     """Rows of 4 M fp32 columns (the plan's width limit: 256 chunks of the
