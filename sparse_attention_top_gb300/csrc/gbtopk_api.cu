@@ -131,9 +131,10 @@ int make_plan(int64_t num_rows, int64_t width, int32_t top_k, int dtype, Plan *p
     pl.det_bytes = det_scratch_bytes(sel_cap);
     pl.row_smem_sorted = pl.off_stage + (stage > pl.det_bytes ? stage : pl.det_bytes);
     // split plans select nothing in the row kernel unless the output is
-    // sorted (short rows are written straight out): the guess's counters and
-    // sample only (12 KB with the control block)
-    pl.row_smem = pl.split ? align_up(pl.off_hist + guess, 128) : pl.off_stage + stage;
+    // sorted (short rows are written straight out): the guess's counters only
+    // (its sample stays in registers; 4 KB with the control block), so three
+    // chunk-kernel blocks fit beside four row-kernel blocks on one SM
+    pl.row_smem = pl.split ? align_up(pl.off_hist + static_cast<size_t>(kGuessBins) * 4, 128) : pl.off_stage + stage;
     if (pl.row_smem_sorted > kMaxSmemBytes) return GBTOPK_EUNSUPPORTED;
     pl.ws_bytes = kWsHeaderBytes + static_cast<size_t>(num_rows) * pl.ws_row_bytes;
     *plan = pl;

@@ -927,8 +927,15 @@ __device__ __forceinline__ void warp_find_two_bins(const uint32_t *hist, uint32_
     }
 }
 
+// A sample's keys as one thread holds them: key j is valid for j < count.
+struct ThreadKeys {
+    static constexpr int kMax = 8;
+    uint32_t key[kMax];
+    int count;
+};
+
 template <int NT, int NB>
-__device__ uint32_t adaptive_threshold(const uint32_t *keys, int m, uint32_t r, uint32_t e, uint32_t kmin,
+__device__ uint32_t adaptive_threshold(const ThreadKeys &tk, uint32_t r, uint32_t e, uint32_t kmin,
                                        uint32_t kmax, uint32_t *hist, Ctrl &c, uint32_t &upper_e) {
     constexpr int NBITS = NB == 512 ? 9 : (NB == 1024 ? 10 : (NB == 2048 ? 11 : 12));
     static_assert((1 << NBITS) == NB, "bin count");
@@ -937,7 +944,9 @@ __device__ uint32_t adaptive_threshold(const uint32_t *keys, int m, uint32_t r, 
 #pragma unroll
     for (int j = 0; j < NB / NT; ++j) hist[threadIdx.x + j * NT] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < m; i += NT) atomicAdd(&hist[(keys[i] - kmin) >> shift], 1u);
+#pragma unroll
+    for (int j = 0; j < ThreadKeys::kMax; ++j)
+        if (j < tk.count) atomicAdd(&hist[(tk.key[j] - kmin) >> shift], 1u);
     __syncthreads();
     if (threadIdx.x == 0) GBTOPK_TRACE_SET(blockIdx.x, 16, -1);  // (row kernel blocks)
     warp_find_two_bins<NB>(hist, e, r, c);
@@ -954,9 +963,10 @@ __device__ uint32_t adaptive_threshold(const uint32_t *keys, int m, uint32_t r, 
 #pragma unroll
     for (int j = 0; j < NB / NT; ++j) hist[threadIdx.x + j * NT] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < m; i += NT) {
-        const uint32_t d = keys[i] - kmin;
-        if ((d >> shift) == b) atomicAdd(&hist[(d - (b << shift)) >> shift2], 1u);
+#pragma unroll
+    for (int j = 0; j < ThreadKeys::kMax; ++j) {
+        const uint32_t d = tk.key[j] - kmin;
+        if (j < tk.count && (d >> shift) == b) atomicAdd(&hist[(d - (b << shift)) >> shift2], 1u);
     }
     __syncthreads();
     if (threadIdx.x == 0) GBTOPK_TRACE_SET(blockIdx.x, 18, -1);
@@ -974,7 +984,7 @@ __device__ uint32_t adaptive_threshold(const uint32_t *keys, int m, uint32_t r, 
 // fine bins even when the keys above it span many binades or both signs;
 // keys far above it pile into the top bins, which are taken whole.
 template <int NT>
-__device__ void guess_from_sample(const uint32_t *sample, int m, int64_t n, int k, uint32_t kmin,
+__device__ void guess_from_sample(const ThreadKeys &sample, int m, int64_t n, int k, uint32_t kmin,
                                   uint32_t kmax, uint32_t *hist, Ctrl &c, uint32_t &t_lo,
                                   int &bin_shift) {
     uint32_t r = guess_rank(n, k);
@@ -982,7 +992,7 @@ __device__ void guess_from_sample(const uint32_t *sample, int m, int64_t n, int 
     uint32_t e = static_cast<uint32_t>((static_cast<int64_t>(m) * k + n - 1) / n);
     e = e < 1u ? 1u : (e > r ? r : e);
     uint32_t t_est;
-    t_lo = adaptive_threshold<NT, kGuessBins>(sample, m, r, e, kmin, kmax, hist, c, t_est);
+    t_lo = adaptive_threshold<NT, kGuessBins>(sample, r, e, kmin, kmax, hist, c, t_est);
     const int bits = 32 - __clz(t_est - t_lo);
     bin_shift = bits > kBinBits - 1 ? bits - (kBinBits - 1) : 0;
 }
@@ -1195,6 +1205,7 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
             reinterpret_cast<uint4 *>(row_hist(p, row))[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
         int m;
         uint32_t kmin = 0xFFFFFFFFu, kmax = 0;
+        ThreadKeys tk;  // this thread's sample keys (registers)
         // hint anchor (the previous argmax column): thread 32 issues its two
         // dependent loads alongside the sample's, and folds the value in
         // after the barrier
@@ -1226,20 +1237,30 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
 #pragma unroll
                 for (int j = 0; j < 8; ++j) raw[j] = ldg_raw(xrow + pos + j);
             }
+            static_assert(ThreadKeys::kMax == 8 && kSampleGroups == kThreads, "one group of 8 per thread");
+            tk.count = 8;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const uint32_t key = Elem<DT>::key(raw[j]);
-                sample[threadIdx.x * 8 + j] = key;
+                tk.key[j] = key;
                 kmin = key < kmin ? key : kmin;
                 kmax = key > kmax ? key : kmax;
             }
         } else {
-            m = static_cast<int>(n);
-            for (int i = threadIdx.x; i < m; i += kThreads) {
-                const uint32_t key = Elem<DT>::key(ldg_raw(xrow + i));
-                sample[i] = key;
-                kmin = key < kmin ? key : kmin;
-                kmax = key > kmax ? key : kmax;
+            m = static_cast<int>(n);  // the whole row: column threadIdx.x + j kThreads
+            static_assert(ThreadKeys::kMax * kThreads >= kSampleSize, "the sample fits the threads' keys");
+            tk.count = 0;
+#pragma unroll
+            for (int j = 0; j < ThreadKeys::kMax; ++j) {
+                const int i = static_cast<int>(threadIdx.x) + j * kThreads;
+                tk.key[j] = 0u;
+                if (i < m) {
+                    const uint32_t key = Elem<DT>::key(ldg_raw(xrow + i));
+                    tk.key[j] = key;
+                    tk.count = j + 1;
+                    kmin = key < kmin ? key : kmin;
+                    kmax = key > kmax ? key : kmax;
+                }
             }
         }
         const bool hint_ok = threadIdx.x == kHintThread &&
@@ -1257,7 +1278,7 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
         GBTOPK_TRACE_POINT(2, 0);
         uint32_t t_lo;
         int bin_shift;
-        guess_from_sample<kThreads>(sample, m, n, k, c.key_min, c.key_max, hist, c, t_lo, bin_shift);
+        guess_from_sample<kThreads>(tk, m, n, k, c.key_min, c.key_max, hist, c, t_lo, bin_shift);
         if (threadIdx.x == 0) {
             uint32_t *info = row_info(p, row);
             info[0] = t_lo;
@@ -1314,10 +1335,18 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
             kmin = key < kmin ? key : kmin;
             kmax = key > kmax ? key : kmax;
         }
-        block_minmax(kmin, kmax, c);
+        block_minmax(kmin, kmax, c);  // (its barrier publishes the sample)
+        ThreadKeys tk;
+        tk.count = 0;
+#pragma unroll
+        for (int j = 0; j < ThreadKeys::kMax; ++j) {
+            const int i = static_cast<int>(threadIdx.x) + j * kThreads;
+            tk.key[j] = i < m ? sample[i] : 0u;
+            if (i < m) tk.count = j + 1;
+        }
         uint32_t t_lo;
         int bin_shift;
-        guess_from_sample<kThreads>(sample, m, n, k, c.key_min, c.key_max, hist, c, t_lo, bin_shift);
+        guess_from_sample<kThreads>(tk, m, n, k, c.key_min, c.key_max, hist, c, t_lo, bin_shift);
 #pragma unroll
         for (int j = 0; j < kBins / kThreads; ++j) hist[threadIdx.x + j * kThreads] = 0;
         __syncthreads();
