@@ -33,12 +33,12 @@ constexpr int kGatherCandidates = 8192; // candidates the finalize kernel gather
 constexpr size_t kMaxSmemBytes = 232448;  // dynamic shared memory one block may opt into (227 KB)
 constexpr int kPairSortMax = 2048;     // sorted output copies up to this many pairs, else 16-bit positions
 constexpr size_t kWsHeaderBytes = 256; // device status word + padding
-constexpr size_t kRowInfoBytes = 16;   // t_lo, bin shift, chunk ticket (written by the row kernel)
+constexpr size_t kRowInfoBytes = 16;   // t_lo, coarse bin shift, chunk ticket (written by the row kernel)
 constexpr uint32_t kSpinLimit = 1u << 22;
-// Coarse candidate bins of a split row's final selection: bin_of's bins
-// taken kCoarseShift bits at a time, the top bin open-ended.
+// Coarse candidate bins of a split row's final selection: keys t_lo .. t_est
+// (the guess and its estimate of the k-th key) fill the lower half of the
+// bins, one key per bin when that range is short, the top bin open-ended.
 constexpr int kCoarseBins = 256;
-constexpr int kCoarseShift = 4;
 
 // Fused split path (top_k <= kPairSortMax): one block of kThreads per chunk
 // of kFusedChunkBytes, finalized in its own shared memory by the row's last

@@ -777,10 +777,9 @@ __device__ __forceinline__ uint32_t bin_of(uint32_t key, uint32_t t_lo, int bin_
     return b < static_cast<uint32_t>(kBins - 1) ? b : static_cast<uint32_t>(kBins - 1);
 }
 
-// Coarse bin of a candidate key (kCoarseShift bits of bin_of at a time; the
-// top bin takes everything above).
-__device__ __forceinline__ uint32_t coarse_bin(uint32_t key, uint32_t t_lo, int bin_shift) {
-    const uint32_t b = (key - t_lo) >> (bin_shift + kCoarseShift);
+// Coarse bin of a candidate key (the top bin takes everything above).
+__device__ __forceinline__ uint32_t coarse_bin(uint32_t key, uint32_t t_lo, int coarse_shift) {
+    const uint32_t b = (key - t_lo) >> coarse_shift;
     return b < static_cast<uint32_t>(kCoarseBins - 1) ? b : static_cast<uint32_t>(kCoarseBins - 1);
 }
 
@@ -986,7 +985,7 @@ __device__ uint32_t adaptive_threshold(const ThreadKeys &tk, uint32_t r, uint32_
 template <int NT>
 __device__ void guess_from_sample(const ThreadKeys &sample, int m, int64_t n, int k, uint32_t kmin,
                                   uint32_t kmax, uint32_t *hist, Ctrl &c, uint32_t &t_lo,
-                                  int &bin_shift) {
+                                  int &bin_shift, int &coarse_shift) {
     uint32_t r = guess_rank(n, k);
     if (r > static_cast<uint32_t>(m)) r = static_cast<uint32_t>(m);
     uint32_t e = static_cast<uint32_t>((static_cast<int64_t>(m) * k + n - 1) / n);
@@ -995,6 +994,9 @@ __device__ void guess_from_sample(const ThreadKeys &sample, int m, int64_t n, in
     t_lo = adaptive_threshold<NT, kGuessBins>(sample, r, e, kmin, kmax, hist, c, t_est);
     const int bits = 32 - __clz(t_est - t_lo);
     bin_shift = bits > kBinBits - 1 ? bits - (kBinBits - 1) : 0;
+    constexpr int kCoarseBits = 8;  // log2(kCoarseBins)
+    static_assert((1 << kCoarseBits) == kCoarseBins, "coarse bins");
+    coarse_shift = bits > kCoarseBits - 1 ? bits - (kCoarseBits - 1) : 0;
 }
 
 
@@ -1278,11 +1280,13 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
         GBTOPK_TRACE_POINT(2, 0);
         uint32_t t_lo;
         int bin_shift;
-        guess_from_sample<kThreads>(tk, m, n, k, c.key_min, c.key_max, hist, c, t_lo, bin_shift);
+        int coarse_shift;
+        guess_from_sample<kThreads>(tk, m, n, k, c.key_min, c.key_max, hist, c, t_lo, bin_shift, coarse_shift);
+        (void)bin_shift;
         if (threadIdx.x == 0) {
             uint32_t *info = row_info(p, row);
             info[0] = t_lo;
-            info[1] = static_cast<uint32_t>(bin_shift);
+            info[1] = static_cast<uint32_t>(coarse_shift);
             info[2] = 0;  // the row's chunk ticket (fused plans)
         }
         GBTOPK_TRACE_POINT(6, 0);
@@ -1346,7 +1350,9 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
         }
         uint32_t t_lo;
         int bin_shift;
-        guess_from_sample<kThreads>(tk, m, n, k, c.key_min, c.key_max, hist, c, t_lo, bin_shift);
+        int coarse_shift;
+        guess_from_sample<kThreads>(tk, m, n, k, c.key_min, c.key_max, hist, c, t_lo, bin_shift, coarse_shift);
+        (void)coarse_shift;
 #pragma unroll
         for (int j = 0; j < kBins / kThreads; ++j) hist[threadIdx.x + j * kThreads] = 0;
         __syncthreads();
@@ -1919,7 +1925,7 @@ __device__ void finalize_row(const Params &p, int64_t row, int64_t n, int64_t co
     const uint32_t my = tid < nch ? __ldcg(row_counts(p, row) + tid) : 0u;
     const uint32_t hcount = (ws_hist && tid < kCoarseBins) ? __ldcg(row_hist(p, row) + tid) : 0u;
     const uint32_t t_lo = info.x;
-    const int bin_shift = static_cast<int>(info.y);
+    const int coarse_shift = static_cast<int>(info.y);
     const uint32_t cap = static_cast<uint32_t>(chunk_seg_cap(n, k, p.plan.chunk));
     const uint2 *segs = row_segs(p, row);
     if (tid < kCoarseBins) c.rhist[tid] = hcount;
@@ -2015,7 +2021,7 @@ __device__ void finalize_row(const Params &p, int64_t row, int64_t n, int64_t co
     if (!fallback) {
         if (!ws_hist) {
             for_each_cand([&](bool live, uint2 v) {
-                if (live) atomicAdd(&c.rhist[coarse_bin(Elem<DT>::key(v.x), t_lo, bin_shift)], 1u);
+                if (live) atomicAdd(&c.rhist[coarse_bin(Elem<DT>::key(v.x), t_lo, coarse_shift)], 1u);
             });
             __syncthreads();
         }
@@ -2024,7 +2030,7 @@ __device__ void finalize_row(const Params &p, int64_t row, int64_t n, int64_t co
         // of the coarse bins above b
         coarse_select(c.rhist, static_cast<uint32_t>(k), c);
         __syncthreads();
-        const int s0 = bin_shift + kCoarseShift;
+        const int s0 = coarse_shift;
         uint32_t b = c.bcast[2];
         above = c.bcast[3];
         bsize = c.bcast[4];
