@@ -2309,8 +2309,8 @@ __global__ void __launch_bounds__(kThreads, 3) chunk_kernel(const __grid_constan
     }
     GBTOPK_TRACE_POINT(3, 0);
     // the chunk's coarse histogram into the row's (one add per nonempty
-    // bin), then the ticket: the barriers and thread 0's fence order every
-    // candidate, count and add of the block before it
+    // bin), then the ticket: the barriers and thread 0's acquire-release
+    // atomic order every candidate, count and add of the block before it
     __syncthreads();
     GBTOPK_TRACE_POINT(16, 0);
     if (ok && c.rhist[tid] != 0u) atomicAdd(row_hist(p, row) + tid, c.rhist[tid]);
@@ -2318,11 +2318,13 @@ __global__ void __launch_bounds__(kThreads, 3) chunk_kernel(const __grid_constan
     GBTOPK_TRACE_POINT(17, 0);
     if (tid == 0) {
         row_counts(p, row)[ch] = ok ? c.sel_count : 0xFFFFFFFFu;  // an unread chunk: the row falls back
-        __threadfence();
         GBTOPK_TRACE_POINT(18, 0);
-        const uint32_t done = atomicAdd(info + 2, 1u);
+        // one acquire-release atomic: releases this block's candidates, count
+        // and histogram adds (ordered before it by the barriers above), and
+        // acquires every earlier block's for the block that completes the row
+        uint32_t done;
+        asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(done) : "l"(info + 2) : "memory");
         const bool is_last = done == static_cast<uint32_t>(nch - 1);
-        if (is_last) __threadfence();  // acquire: every chunk's candidates, counts and histogram
         c.bcast[6] = is_last ? 1u : 0u;
     }
     __syncthreads();
