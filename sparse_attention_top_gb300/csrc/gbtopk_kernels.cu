@@ -1199,6 +1199,10 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
     }
 
     if (n > p.plan.direct_max) {
+        // the chunk / stream kernel may launch at once: its bulk copies of the
+        // row then overlap this guess (it reads the guess only once this grid
+        // has completed)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         // ---- split row: threshold guess from a strided sample (the whole
         // row when it has at most kSampleSize columns).  First clear the
         // row's coarse candidate histogram, which the chunk kernel counts
@@ -1271,7 +1275,6 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
         if (hint_ok) hraw = ldg_raw(xrow + a);
         __syncthreads();
         GBTOPK_TRACE_POINT(1, 0);
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         if (hint_ok) {
             const uint32_t key = Elem<DT>::key(hraw);
             kmax = key > kmax ? key : kmax;
