@@ -7,8 +7,10 @@
 // `top_k_varlen` seq_lens formula or from the page-table calls' lengths and
 // row_starts):
 //   * n == 0 or n <= k -> every valid column, then -1 (short path);
-//   * widths up to 2048 without the sorted order: one warp per row
-//     (small_kernel, a warp-private radix select on keys in registers);
+//   * widths up to 2048 without the sorted order: one warp per row, a
+//     warp-private radix select (small16_kernel for 16-bit rows: the row
+//     staged by one bulk copy and turned into packed pair keys in place;
+//     small_kernel for fp32: keys in registers);
 //   * rows of up to 64 KB: one block per row (row_kernel): the
 //     row is staged in shared memory by one bulk copy, a threshold is
 //     guessed from a strided sample, the elements at or above it are kept
@@ -21,8 +23,8 @@
 //     the row's last block (atomic ticket) selects the row in its own
 //     shared memory (finalize_row);
 //   * other split plans: row_kernel's guesses, then the persistent
-//     stream_kernel filters every chunk through a bulk-copy ring, then
-//     final_kernel selects each row (finalize_row).
+//     stream_kernel filters every 64 KB chunk through a bulk-copy ring of
+//     three stages, then final_kernel selects each row (finalize_row).
 // The three launches of a call are chained by programmatic dependent launch.
 // A guess that was too high, a candidate segment that overflowed or a
 // bounded wait that gave up sends the row through an exact radix select
