@@ -7,6 +7,7 @@ strided score views, degenerate hints, deterministic mode, the compact
 page-table transform, output canaries, a poisoned scratch workspace and CUDA
 graph replay with changing lengths.
 """
+import dataclasses
 import warnings
 
 import numpy as np
@@ -216,6 +217,32 @@ def test_small_rows_page_table(dev):
     c = workloads.page_table_case(rows=48, width=1500, row_stride=1531, page_size=16,
                                   pt_cols=128, top_k=256, deterministic=False, seed=5077)
     _run_page_table(dev, c)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_small_rows_16bit_epilogues(dev, dtype):
+    """The 16-bit one-warp rows with the page-table epilogue (out and out_raw,
+    ragged row starts, an odd row stride so rows start at any element) and
+    with the ragged-offset epilogue."""
+    c = workloads.page_table_case(rows=48, width=1800, row_stride=1831, page_size=16,
+                                  pt_cols=160, top_k=256, deterministic=False, seed=5078)
+    storage = torch.as_strided(c.scores, (48, 1831), (1831, 1)).to(dtype)
+    c = dataclasses.replace(c, scores=storage[:, :1800])
+    _run_page_table(dev, c)
+    R, W, k = 40, 1800, 300
+    scores, lengths, starts = _ragged_case(R, W, 7400, dtype=dtype, stride=W + 5)
+    g = torch.Generator().manual_seed(13)
+    offsets = torch.randint(-1000, 10_000_000, (R,), generator=g, dtype=torch.int32)
+    out = gb.top_k_ragged_transform(_to_dev_strided(scores, dev), lengths.to(dev), offsets.to(dev), k,
+                                    row_starts=starts.to(dev))
+    torch.cuda.synchronize(dev)
+    ref = oracle.ragged_offset_transform(scores, lengths, offsets, k, starts)
+    raw = out.cpu().clone()
+    raw[raw >= 0] -= offsets.view(-1, 1).expand_as(raw)[raw >= 0]
+    refraw = ref.clone()
+    refraw[ref >= 0] -= offsets.view(-1, 1).expand_as(ref)[ref >= 0]
+    n = [oracle.ragged_length(int(lengths[r]), int(starts[r]), W) for r in range(R)]
+    check_rows(scores, n, k, raw, refraw, None, col0=starts.tolist())
 
 
 def test_misaligned_and_strided_views(dev):
