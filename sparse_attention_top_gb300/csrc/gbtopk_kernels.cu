@@ -605,6 +605,18 @@ __device__ __forceinline__ void put_slot(const Params &p, int64_t row, const Row
 template <int DT>
 __device__ void emit(const Params &p, int64_t row, const uint2 *sel, int m) {
     const RowEpi ep = row_epilogue(p, row);
+    int32_t *orow = p.out_idx + row * p.k;
+    if (!p.out_raw && !p.out_val && !p.page_table && !p.idx_offset && m == p.k && (p.k & 3) == 0 &&
+        (reinterpret_cast<uintptr_t>(orow) & 15u) == 0u) {
+        // four slots per thread and store: 16-byte stores of the column indices
+        for (int j = threadIdx.x * 4; j < p.k; j += blockDim.x * 4) {
+            const uint4 a = *reinterpret_cast<const uint4 *>(sel + j);
+            const uint4 b = *reinterpret_cast<const uint4 *>(sel + j + 2);
+            *reinterpret_cast<int4 *>(orow + j) = make_int4(static_cast<int>(a.y), static_cast<int>(a.w),
+                                                            static_cast<int>(b.y), static_cast<int>(b.w));
+        }
+        return;
+    }
 #pragma unroll 4
     for (int j = threadIdx.x; j < p.k; j += blockDim.x) {
         const bool live = j < m;

@@ -94,6 +94,23 @@ def test_dsv32_full(dev, hinted):
     run_case(dev, c, det=False)
 
 
+@pytest.mark.parametrize("name", ["decode", "mtp", "sweep"])
+def test_indices_only(dev, name):
+    """Calls that write indices alone (no values, raw indices or epilogue), as
+    the benchmark makes them: the selection's 16-byte index stores on the
+    two-kernel and ring paths."""
+    if name == "decode":
+        c = workloads.dsv32_decode(rows=64, width=163840, top_k=2048, hinted=True)
+        rows = None
+    elif name == "mtp":
+        c = workloads.dsv4_mtp(requests=64, width=65536)
+        rows = None
+    else:
+        c = workloads.long_row_sweep(256, 2048, True, seed=3999)
+        rows = [0, 1, 2, 100, 127, 128, 200, 254, 255]
+    run_case(dev, c, rows=rows, poison=False, values=False)
+
+
 @pytest.mark.parametrize("rows,k,hinted", [(1, 2048, True), (16, 512, False), (16, 1024, True),
                                            (64, 2048, False), (256, 1024, True),
                                            (1024, 2048, True)])
