@@ -162,6 +162,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Byte permute (PTX prmt, generic mode): selector nibble i picks, for result byte i,
+// one of the bytes 0-7 of {b, a}; a nibble with bit 3 set replicates that byte's
+// sign bit over the result byte.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
 // Claims consecutive slots of a shared counter for the lanes with `pred`
 // (one atomic per warp).  Every lane of the warp must call it.
 __device__ __forceinline__ uint32_t warp_claim(uint32_t *counter, bool pred) {
@@ -823,24 +832,22 @@ struct PassTest {
         if (Elem<DT>::kBytes == 4) return __uint_as_float(raw) >= tf;
         return Elem<DT>::key(raw) >= t_lo;
     }
-    __device__ __forceinline__ static uint32_t pair_bits(uint32_t m) {  // 0xFFFF halves -> 2 bits
-        return (m & 1u) | ((m >> 15) & 2u);
-    }
-    __device__ __forceinline__ uint32_t pair_mask(uint32_t word) const {
+    // 0xFFFF in each half of the packed pair `word` that is >= the threshold
+    __device__ __forceinline__ uint32_t pair_ge_mask(uint32_t word) const {
         if constexpr (DT == 1) {
             __nv_bfloat162_raw a, b;
             a.x = static_cast<unsigned short>(word & 0xFFFFu);
             a.y = static_cast<unsigned short>(word >> 16);
             b.x = static_cast<unsigned short>(t2 & 0xFFFFu);
             b.y = static_cast<unsigned short>(t2 >> 16);
-            return pair_bits(__hge2_mask(__nv_bfloat162(a), __nv_bfloat162(b)));
+            return __hge2_mask(__nv_bfloat162(a), __nv_bfloat162(b));
         } else {
             __half2_raw a, b;
             a.x = static_cast<unsigned short>(word & 0xFFFFu);
             a.y = static_cast<unsigned short>(word >> 16);
             b.x = static_cast<unsigned short>(t2 & 0xFFFFu);
             b.y = static_cast<unsigned short>(t2 >> 16);
-            return pair_bits(__hge2_mask(__half2(a), __half2(b)));
+            return __hge2_mask(__half2(a), __half2(b));
         }
     }
     __device__ __forceinline__ uint32_t mask(const uint4 &w) const {
@@ -850,7 +857,12 @@ struct PassTest {
                    (static_cast<uint32_t>(__uint_as_float(w.z) >= tf) << 2) |
                    (static_cast<uint32_t>(__uint_as_float(w.w) >= tf) << 3);
         } else {
-            return pair_mask(w.x) | (pair_mask(w.y) << 2) | (pair_mask(w.z) << 4) | (pair_mask(w.w) << 6);
+            // the top byte of each compared half (0xFF or 0) into one byte per
+            // element, then the bytes' top bits gathered by one multiply (bits
+            // 7, 15, 23, 31 land on 28-31; no two partial products overlap)
+            const uint32_t lo = prmt(pair_ge_mask(w.x), pair_ge_mask(w.y), 0x7531u) & 0x80808080u;
+            const uint32_t hi = prmt(pair_ge_mask(w.z), pair_ge_mask(w.w), 0x7531u) & 0x80808080u;
+            return ((lo * 0x00204081u) >> 28) | (((hi * 0x00204081u) >> 28) << 4);
         }
     }
 };
@@ -2492,15 +2504,6 @@ __global__ void __launch_bounds__(128) small_kernel(const __grid_constant__ Para
             out[j] = out_index(p, ep, idx);
         }
     }
-}
-
-// Byte permute (PTX prmt, generic mode): selector nibble q picks byte q of
-// {b, a} for result byte i; a nibble with bit 3 set replicates that byte's
-// sign bit over the result byte.
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
 }
 
 // Elem16::key of both halves of a word at once: a half whose magnitude is
