@@ -1,8 +1,8 @@
 """GPU parity: the CUDA path against the CPU oracle, through the C ABI.
 
 Covers the five workloads (reduced and at full size), the split / direct /
-short / empty row paths, ties, signed zeros, infinities, denormals, poisoned
-padding (TensorRT-LLM PR #17821, "padding poisoned with 3e38"), misaligned and
+short / empty row paths, ties, signed zeros, infinities, denormals, padding
+past each row's length filled with 3e38 (as TensorRT-LLM PR #17821 tests it), misaligned and
 strided score views, degenerate hints, deterministic mode, the compact
 page-table transform, output canaries, a poisoned scratch workspace and CUDA
 graph replay with changing lengths.
