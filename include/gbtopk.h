@@ -160,9 +160,9 @@ int gbtopk_page_table_transform(const void *scores, int dtype, int64_t num_rows,
 /*
  * gbtopk_ragged_transform — top-K fused with the ragged KV index offset.
  *
- * Defined by the SGLang TopK ops wiki, fast_topk_transform_ragged_fused
- * ("top-k indices ... offset-adjusted for ragged KV layout", with
- * topk_indices_offset of shape (B)): the selection is the one of
+ * Defined by the SGLang TopK ops wiki, fast_topk_transform_ragged_fused (its
+ * top-k indices shifted by a per-row offset for a ragged KV layout, the
+ * offsets topk_indices_offset of shape (B)): the selection is the one of
  * gbtopk_page_table_transform's rows, and each selected row-local index idx
  * is written as idx + topk_indices_offset[r] (modulo 2^32); -1 padding stays
  * -1.
