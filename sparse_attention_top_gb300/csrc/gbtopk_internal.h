@@ -16,7 +16,7 @@ constexpr int kSampleGroups = 256;     // one group of 8 consecutive columns per
 constexpr int kSampleSize = kSampleGroups * 8;
 constexpr int kBinBits = 12;
 constexpr int kBins = 1 << kBinBits;   // candidate histogram bins
-constexpr int kGuessBins = 512;        // bins of each round of the sample's threshold search
+constexpr int kGuessBins = 1024;       // bins of the sample's threshold search (each round)
 constexpr int kRankMax = 256;          // boundary-bin size resolved by rank counting
 constexpr int kRankAllMax = 64;        // the same in the finalize (a block radix select above)
 constexpr size_t kCtrlBytes = 2048;    // per-block control block (counters, scan, digit histogram)

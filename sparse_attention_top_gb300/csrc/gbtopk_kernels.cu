@@ -193,6 +193,17 @@ __device__ __forceinline__ void warp_hist_add(uint32_t *hist, uint32_t bin, bool
     }
 }
 
+// Inclusive prefix sum over the lanes of a full warp.
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
+    const uint32_t lane = lane_id();
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= static_cast<uint32_t>(off)) v += y;
+    }
+    return v;
+}
+
 // Exclusive prefix sum of one value per thread (thread order).  All threads.
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, Ctrl &c, uint32_t &total) {
     const uint32_t lane = lane_id(), warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -905,49 +916,41 @@ __device__ void find_bin_from_top(const uint32_t *hist, uint32_t r, Ctrl &c) {
 // Warp 0: for ranks r0 and r1 (1-based, <= the total count), the bins of
 // hist[NB] holding the r0-th and r1-th largest items: c.bcast[2 + 3i] = the
 // bin, c.bcast[3 + 3i] = the count above it, c.bcast[4 + 3i] = its count
-// (i = 0, 1).  Lane l holds bins NB - 1 - (NB / 32) l - j.  The caller syncs
-// the block after it.
+// (i = 0, 1).  Lane l first sums the run of PER = NB / 32 bins below
+// NB - PER l (vector loads) and one warp scan finds the run holding each
+// rank; then lane j reads the j-th bin from the top of that run and a
+// second warp scan finds the bin (no counter array held per lane).  The
+// caller syncs the block after it.
 template <int NB>
 __device__ __forceinline__ void warp_find_two_bins(const uint32_t *hist, uint32_t r0, uint32_t r1, Ctrl &c) {
     constexpr int PER = NB / 32;
+    static_assert(PER % 4 == 0 && PER <= 32, "vector loads, one bin per lane of a run");
     if (threadIdx.x >= 32) return;
     const uint32_t lane = lane_id();
-    static_assert(PER % 4 == 0, "vector loads");
-    uint32_t cnt[PER], s = 0;
     const uint4 *h4 = reinterpret_cast<const uint4 *>(hist + NB - PER * (static_cast<int>(lane) + 1));
+    uint32_t s = 0;
 #pragma unroll
     for (int q = 0; q < PER / 4; ++q) {
         const uint4 v = h4[q];
-        cnt[PER - 1 - 4 * q] = v.x;
-        cnt[PER - 2 - 4 * q] = v.y;
-        cnt[PER - 3 - 4 * q] = v.z;
-        cnt[PER - 4 - 4 * q] = v.w;
+        s += (v.x + v.y) + (v.z + v.w);
     }
-#pragma unroll
-    for (int j = 0; j < PER; ++j) s += cnt[j];
-    uint32_t incl = s;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= static_cast<uint32_t>(off)) incl += y;
-    }
+    const uint32_t incl = warp_incl_scan(s);
     const uint32_t excl = incl - s;
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const uint32_t r = i == 0 ? r0 : r1;
         const uint32_t bal = __ballot_sync(0xffffffffu, excl < r && r <= incl);
-        if (bal != 0u && static_cast<int>(lane) == __ffs(bal) - 1) {
-            uint32_t acc = excl;
-#pragma unroll
-            for (int j = 0; j < PER; ++j) {
-                if (acc + cnt[j] >= r) {
-                    c.bcast[2 + 3 * i] = static_cast<uint32_t>(NB - 1 - PER * static_cast<int>(lane) - j);
-                    c.bcast[3 + 3 * i] = acc;
-                    c.bcast[4 + 3 * i] = cnt[j];
-                    break;
-                }
-                acc += cnt[j];
-            }
+        if (bal == 0u) continue;  // (warp-uniform) r above the total
+        const int owner = __ffs(bal) - 1;
+        const uint32_t base = __shfl_sync(0xffffffffu, excl, owner);
+        const int top = NB - 1 - PER * owner;  // the run's top bin
+        const uint32_t cnt = static_cast<int>(lane) < PER ? hist[top - static_cast<int>(lane)] : 0u;
+        const uint32_t in2 = base + warp_incl_scan(cnt);
+        const uint32_t f = __ffs(__ballot_sync(0xffffffffu, in2 >= r)) - 1;  // a lane < PER
+        if (lane == f) {
+            c.bcast[2 + 3 * i] = static_cast<uint32_t>(top - static_cast<int>(f));
+            c.bcast[3 + 3 * i] = in2 - cnt;
+            c.bcast[4 + 3 * i] = cnt;
         }
     }
 }
@@ -1000,6 +1003,91 @@ __device__ uint32_t adaptive_threshold(const ThreadKeys &tk, uint32_t r, uint32_
     return edge + (c.bcast[2] << shift2);
 }
 
+// The value whose key (Elem<DT>::key) is `key`, widened to float (exact for
+// every value of the three types; both zeros give +0).
+template <int DT>
+__device__ __forceinline__ float key_value(uint32_t key) {
+    if constexpr (DT == 0) {
+        return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+    } else {
+        const uint32_t raw = (key & 0x8000u) ? (key & 0x7FFFu) : (~key & 0xFFFFu);
+        if constexpr (DT == 1) {
+            return __uint_as_float(raw << 16);
+        } else {
+            return __half2float(__ushort_as_half(static_cast<unsigned short>(raw)));
+        }
+    }
+}
+
+// Conservative rank-r threshold of the sample over bins of equal VALUE
+// width: NB bins spanning the sample's value range [value(kmin),
+// value(kmax)].  The bin of a key is a nondecreasing function of its value
+// (rounded subtract, multiply and truncation are all monotone), and key
+// order is value order, so every key in a higher bin is larger than every
+// key in a lower one.  Warp 0 finds the bins holding the e-th and r-th
+// largest keys; one more pass takes the smallest key of the r-th's bin as
+// the threshold (at least r keys are >= it) and the largest key of the
+// e-th's bin as the upper estimate of the e-th key.  Where the sample is
+// dense, value bins hold a few keys each, while bins of equal key width
+// follow the binades and crowd the sample into a few dozen bins, so the
+// single round here replaces adaptive_threshold's two.  That function is
+// still taken when the value range is not a finite positive span, or when
+// the r-th's bin holds more than max(16, r / 8) keys (a wide range around a
+// dense cluster), which would leave the threshold too far below the r-th
+// key.
+template <int DT, int NT, int NB>
+__device__ uint32_t value_threshold(const ThreadKeys &tk, uint32_t r, uint32_t e, uint32_t kmin, uint32_t kmax,
+                                    uint32_t *hist, Ctrl &c, uint32_t &upper_e) {
+    constexpr float kFltMax = 3.402823466e38f;
+    const float vmin = key_value<DT>(kmin);
+    const float span = __fsub_rn(key_value<DT>(kmax), vmin);
+    const float scale = span > 0.0f ? __fdiv_rn(static_cast<float>(NB), span) : 0.0f;
+    auto bin_of_key = [&](uint32_t key) {
+        const int q = __float2int_rz(__fmul_rn(__fsub_rn(key_value<DT>(key), vmin), scale));
+        return static_cast<uint32_t>(q < 0 ? 0 : (q > NB - 1 ? NB - 1 : q));
+    };
+    // block-uniform from here on
+    bool by_keys = !(span > 0.0f && span <= kFltMax && scale > 0.0f && scale <= kFltMax);
+    uint32_t t = 0;
+    if (!by_keys) {
+#pragma unroll
+        for (int j = 0; j < NB / NT; ++j) hist[threadIdx.x + j * NT] = 0;
+        if (threadIdx.x == 0) {
+            c.bcast[0] = 0xFFFFFFFFu;  // smallest key of the r-th's bin
+            c.bcast[1] = 0u;           // largest key of the e-th's bin
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < ThreadKeys::kMax; ++j)
+            if (j < tk.count) atomicAdd(&hist[bin_of_key(tk.key[j])], 1u);
+        __syncthreads();
+        if (threadIdx.x == 0) GBTOPK_TRACE_SET(blockIdx.x, 16, -1);  // (row kernel blocks)
+        warp_find_two_bins<NB>(hist, e, r, c);
+        __syncthreads();
+        if (threadIdx.x == 0) GBTOPK_TRACE_SET(blockIdx.x, 17, -1);
+        const uint32_t be = c.bcast[2];
+        const uint32_t b = c.bcast[5];
+        const uint32_t lim = r / 8u > 16u ? r / 8u : 16u;
+        by_keys = c.bcast[7] > lim;
+        if (!by_keys) {
+#pragma unroll
+            for (int j = 0; j < ThreadKeys::kMax; ++j) {
+                if (j < tk.count) {
+                    const uint32_t q = bin_of_key(tk.key[j]);
+                    if (q == b) atomicMin(&c.bcast[0], tk.key[j]);
+                    if (q == be) atomicMax(&c.bcast[1], tk.key[j]);
+                }
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) GBTOPK_TRACE_SET(blockIdx.x, 18, -1);
+            upper_e = c.bcast[1];
+            t = c.bcast[0];
+        }
+    }
+    if (by_keys) t = adaptive_threshold<NT, NB>(tk, r, e, kmin, kmax, hist, c, upper_e);
+    return t;
+}
+
 // The guess from a sample of m keys (with their min and max) of a row of n
 // columns: t_lo such that, with high probability, at least k row elements
 // are >= t_lo (the sample rank r = e + 6 sqrt(e) + 2, e = m k / n); and the
@@ -1008,7 +1096,7 @@ __device__ uint32_t adaptive_threshold(const ThreadKeys &tk, uint32_t r, uint32_
 // (where the k-th key of the row is expected), so the k-th key lands in
 // fine bins even when the keys above it span many binades or both signs;
 // keys far above it pile into the top bins, which are taken whole.
-template <int NT>
+template <int DT, int NT>
 __device__ void guess_from_sample(const ThreadKeys &sample, int m, int64_t n, int k, uint32_t kmin,
                                   uint32_t kmax, uint32_t *hist, Ctrl &c, uint32_t &t_lo,
                                   int &bin_shift, int &coarse_shift) {
@@ -1017,7 +1105,7 @@ __device__ void guess_from_sample(const ThreadKeys &sample, int m, int64_t n, in
     uint32_t e = static_cast<uint32_t>((static_cast<int64_t>(m) * k + n - 1) / n);
     e = e < 1u ? 1u : (e > r ? r : e);
     uint32_t t_est;
-    t_lo = adaptive_threshold<NT, kGuessBins>(sample, r, e, kmin, kmax, hist, c, t_est);
+    t_lo = value_threshold<DT, NT, kGuessBins>(sample, r, e, kmin, kmax, hist, c, t_est);
     const int bits = 32 - __clz(t_est - t_lo);
     bin_shift = bits > kBinBits - 1 ? bits - (kBinBits - 1) : 0;
     constexpr int kCoarseBits = 8;  // log2(kCoarseBins)
@@ -1310,7 +1398,7 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
         uint32_t t_lo;
         int bin_shift;
         int coarse_shift;
-        guess_from_sample<kThreads>(tk, m, n, k, c.key_min, c.key_max, hist, c, t_lo, bin_shift, coarse_shift);
+        guess_from_sample<DT, kThreads>(tk, m, n, k, c.key_min, c.key_max, hist, c, t_lo, bin_shift, coarse_shift);
         (void)bin_shift;
         if (threadIdx.x == 0) {
             uint32_t *info = row_info(p, row);
@@ -1380,7 +1468,7 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
         uint32_t t_lo;
         int bin_shift;
         int coarse_shift;
-        guess_from_sample<kThreads>(tk, m, n, k, c.key_min, c.key_max, hist, c, t_lo, bin_shift, coarse_shift);
+        guess_from_sample<DT, kThreads>(tk, m, n, k, c.key_min, c.key_max, hist, c, t_lo, bin_shift, coarse_shift);
         (void)coarse_shift;
 #pragma unroll
         for (int j = 0; j < kBins / kThreads; ++j) hist[threadIdx.x + j * kThreads] = 0;
