@@ -53,8 +53,13 @@ constexpr int kTraceFinal = 40960;
 constexpr int kTraceChunk = 8192;  // chunk kernel blocks (up to 24576 of them)
 
 #ifdef GBTOPK_TRACE
-// Phase timestamps (%globaltimer, ns) of the first kTraceBlocks blocks, for
-// builds compiled with -DGBTOPK_TRACE (read back by gbtopk_trace_read).
+// Phase stamps of the first kTraceBlocks blocks, for builds compiled with
+// -DGBTOPK_TRACE (read back by gbtopk_trace_read): SM cycles (%clock64),
+// cheap to read.  Each block also leaves one anchor at its end, slot 30 =
+// %clock64 and slot 31 = %globaltimer (ns) read together, which places its
+// cycle stamps on the common time axis.  A %globaltimer read slows the
+// warp that makes it for thousands of cycles afterwards, so it is taken
+// once per block, after the traced work.
 constexpr int kTraceBlocks = 1 << 16;
 __device__ unsigned long long g_trace[kTraceBlocks][32];
 // Each kernel declares kTraceBase: its blocks use g_trace[kTraceBase + block].
@@ -62,18 +67,28 @@ __device__ unsigned long long g_trace[kTraceBlocks][32];
     do {                                                                                     \
         if (threadIdx.x == 0 && kTraceBase + blockIdx.x < kTraceBlocks) {                    \
             unsigned long long t_;                                                           \
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                           \
+            asm volatile("mov.u64 %0, %%clock64;" : "=l"(t_));                               \
             g_trace[kTraceBase + blockIdx.x][slot] = ((slot) == 7 || (slot) == 15) ? (value) : t_; \
         }                                                                                    \
     } while (0)
-// g_trace[index][slot] = the current time (value < 0) or value, from any thread.
+// g_trace[index][slot] = the current cycle count (value < 0) or value, from any thread.
 #define GBTOPK_TRACE_SET(index, slot, value)                                              \
     do {                                                                                 \
         if ((index) < kTraceBlocks) {                                                    \
             long long v_ = (value);                                                      \
-            if (v_ < 0) asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(v_));          \
+            if (v_ < 0) asm volatile("mov.u64 %0, %%clock64;" : "=l"(v_));              \
             g_trace[(index)][(slot)] = static_cast<unsigned long long>(v_);              \
         }                                                                                \
+    } while (0)
+// The block's anchor (thread 0, at the end of the block's traced work).
+#define GBTOPK_TRACE_ANCHOR()                                                                \
+    do {                                                                                     \
+        if (threadIdx.x == 0 && kTraceBase + blockIdx.x < kTraceBlocks) {                    \
+            unsigned long long c_, g_;                                                       \
+            asm volatile("mov.u64 %0, %%clock64;\n\tmov.u64 %1, %%globaltimer;" : "=l"(c_), "=l"(g_)); \
+            g_trace[kTraceBase + blockIdx.x][30] = c_;                                       \
+            g_trace[kTraceBase + blockIdx.x][31] = g_;                                       \
+        }                                                                                    \
     } while (0)
 #else
 #define GBTOPK_TRACE_POINT(slot, value) \
@@ -81,6 +96,9 @@ __device__ unsigned long long g_trace[kTraceBlocks][32];
     } while (0)
 #define GBTOPK_TRACE_SET(index, slot, value) \
     do {                                     \
+    } while (0)
+#define GBTOPK_TRACE_ANCHOR() \
+    do {                      \
     } while (0)
 #endif
 
@@ -1408,6 +1426,7 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
         }
         GBTOPK_TRACE_POINT(6, 0);
         GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | 3u);
+        GBTOPK_TRACE_ANCHOR();
         return;
     }
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1428,6 +1447,7 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
         }
         GBTOPK_TRACE_POINT(6, 0);
         GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | 1u);
+        GBTOPK_TRACE_ANCHOR();
         return;
     }
 
@@ -1503,6 +1523,7 @@ __global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : 1) row_kernel(const _
     }
     GBTOPK_TRACE_POINT(6, 0);
     GBTOPK_TRACE_POINT(7, (static_cast<unsigned long long>(n) << 8) | 2u);
+    GBTOPK_TRACE_ANCHOR();
     }
 }
 
@@ -1777,9 +1798,7 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
             g_trace[kTraceBase + blockIdx.x][8] = t_wait;
             g_trace[kTraceBase + blockIdx.x][9] = t_busy;
             g_trace[kTraceBase + blockIdx.x][10] = n_items;
-            unsigned long long t_;
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));
-            g_trace[kTraceBase + blockIdx.x][11] = t_;
+            g_trace[kTraceBase + blockIdx.x][11] = clock64();
         }
     #endif
     }
@@ -1796,6 +1815,7 @@ __global__ void __launch_bounds__(kStreamThreads) stream_kernel(const __grid_con
                 atomicOr(reinterpret_cast<uint32_t *>(p.ws), kStatusCopyLost);
     }
     GBTOPK_TRACE_POINT(6, 0);
+    GBTOPK_TRACE_ANCHOR();
 }
 
 
@@ -2072,6 +2092,9 @@ __device__ void finalize_row(const Params &p, int64_t row, int64_t n, int64_t co
     const bool in_smem = total_p <= fr.gather_cap;
     const bool gathered = !fallback && in_smem;  // block-uniform
     bool copy_ok = true;
+    // the coarse window from the workspace counters needs no candidate: on
+    // the gathered path warp 0 finds it while the copies are in flight
+    const bool window_early = gathered && ws_hist;
     if (tid == 0) GBTOPK_TRACE_SET(trace_idx, 8, -1);
     if (gathered) {
         // ---- gather the segments into shared memory (one bulk copy per chunk)
@@ -2088,6 +2111,7 @@ __device__ void finalize_row(const Params &p, int64_t row, int64_t n, int64_t co
                 "l"(segs + static_cast<int64_t>(tid) * cap), "r"(padded * 8u), "r"(smem_u32(bar))
                 : "memory");
         }
+        if (window_early) coarse_select(c.rhist, static_cast<uint32_t>(k), c);  // (published by wait_bar's barrier)
         copy_ok = wait_bar(p.ws, c, bar, parity, p.wait_polls);
         if (tid == 0) GBTOPK_TRACE_SET(trace_idx, 9, -1);
         if (copy_ok) {
@@ -2143,10 +2167,11 @@ __device__ void finalize_row(const Params &p, int64_t row, int64_t n, int64_t co
             __syncthreads();
         }
         // ---- the window [w_lo, w_lo + 2^wbits) holding the k-th key, `above`
-        // candidates above it (wbits 32: open above); fr.fill[b] = the count
-        // of the coarse bins above b
-        coarse_select(c.rhist, static_cast<uint32_t>(k), c);
-        __syncthreads();
+        // candidates above it (wbits 32: open above)
+        if (!window_early) {
+            coarse_select(c.rhist, static_cast<uint32_t>(k), c);
+            __syncthreads();
+        }
         const int s0 = coarse_shift;
         uint32_t b = c.bcast[2];
         above = c.bcast[3];
@@ -2307,6 +2332,7 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(const __grid_const
     finalize_row<DT, kFinalThreads>(p, row, n, col0, nch, fr, &c.bar, 0, false, aborted, c,
                                     kTraceFinal + blockIdx.x);
     GBTOPK_TRACE_POINT(6, 0);
+    GBTOPK_TRACE_ANCHOR();
 }
 
 // Chunk kernel (split rows of plans with top_k <= kPairSortMax): one block
@@ -2459,7 +2485,10 @@ __global__ void __launch_bounds__(kThreads, 3) chunk_kernel(const __grid_constan
         __syncthreads();
         stage_ok = c.bcast[7] != 0;
     }
-    if (!last) return;
+    if (!last) {
+        GBTOPK_TRACE_ANCHOR();
+        return;
+    }
     if (!stage_ok) return;  // the row's outputs stay unwritten; the status word says so
     FinalRegion fr;
     fr.hist = nullptr;
@@ -2472,6 +2501,7 @@ __global__ void __launch_bounds__(kThreads, 3) chunk_kernel(const __grid_constan
     fr.gather_cap = kFusedGatherCap;
     fr.scratch = stage;  // det_scratch_bytes(2048) = 40 KB, below the selection
     finalize_row<DT, kThreads>(p, row, n, col0, nch, fr, &c.bar, 1, true, false, c, kTraceChunk + blockIdx.x);
+    GBTOPK_TRACE_ANCHOR();
 }
 
 // ---------------------------------------------------------------- small rows
@@ -2819,6 +2849,7 @@ __global__ void __launch_bounds__(128, 7) small16_kernel(const __grid_constant__
     }
     GBTOPK_TRACE_POINT(4, 0);
     GBTOPK_TRACE_POINT(7, static_cast<unsigned long long>(n));
+    GBTOPK_TRACE_ANCHOR();
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (!p.page_table && !p.idx_offset && !p.out_val) return;
     __syncwarp();  // the warp's index stores are visible to its lanes
