@@ -1037,47 +1037,62 @@ __device__ __forceinline__ float key_value(uint32_t key) {
     }
 }
 
+// The key of value v rounded down (up) to the element type: every element
+// whose value is >= v (<= v) has a key >= (<=) the result.
+template <int DT>
+__device__ __forceinline__ uint32_t key_of_value(float v, bool up) {
+    if constexpr (DT == 0) {
+        return Elem<DT>::key(__float_as_uint(v));
+    } else if constexpr (DT == 1) {
+        const __nv_bfloat16 h = up ? __float2bfloat16_ru(v) : __float2bfloat16_rd(v);
+        return Elem<DT>::key(__bfloat16_as_ushort(h));
+    } else {
+        const __half h = up ? __float2half_ru(v) : __float2half_rd(v);
+        return Elem<DT>::key(__half_as_ushort(h));
+    }
+}
+
 // Conservative rank-r threshold of the sample over bins of equal VALUE
 // width: NB bins spanning the sample's value range [value(kmin),
 // value(kmax)].  The bin of a key is a nondecreasing function of its value
 // (rounded subtract, multiply and truncation are all monotone), and key
-// order is value order, so every key in a higher bin is larger than every
-// key in a lower one.  Warp 0 finds the bins holding the e-th and r-th
-// largest keys; one more pass takes the smallest key of the r-th's bin as
-// the threshold (at least r keys are >= it) and the largest key of the
-// e-th's bin as the upper estimate of the e-th key.  Where the sample is
-// dense, value bins hold a few keys each, while bins of equal key width
-// follow the binades and crowd the sample into a few dozen bins, so the
-// single round here replaces adaptive_threshold's two.  That function is
-// still taken when the value range is not a finite positive span, or when
-// the r-th's bin holds more than max(16, r / 8) keys (a wide range around a
-// dense cluster), which would leave the threshold too far below the r-th
-// key.
+// order is value order.  Warp 0 finds the bins holding the e-th and r-th
+// largest keys; the threshold is the key of the r-th's bin's lower value
+// edge less half a bin (the margin covers the rounding of the bin map, so
+// at least r keys are >= it), the upper estimate of the e-th key that of
+// its bin's upper edge.  Where the sample is dense, value bins hold a few
+// keys each, while bins of equal key width follow the binades and crowd
+// the sample into a few dozen bins, so one round here does the work of
+// adaptive_threshold's two.  That function is still taken when the value
+// range is not a finite positive span at least 1/256 of the largest
+// magnitude (where the half-bin margin would not cover the rounding), or
+// when the r-th's bin holds more than max(16, r / 8) keys (a wide range
+// around a dense cluster), which would leave the threshold too far below
+// the r-th key.
 template <int DT, int NT, int NB>
 __device__ uint32_t value_threshold(const ThreadKeys &tk, uint32_t r, uint32_t e, uint32_t kmin, uint32_t kmax,
                                     uint32_t *hist, Ctrl &c, uint32_t &upper_e) {
     constexpr float kFltMax = 3.402823466e38f;
     const float vmin = key_value<DT>(kmin);
-    const float span = __fsub_rn(key_value<DT>(kmax), vmin);
+    const float vmax = key_value<DT>(kmax);
+    const float span = __fsub_rn(vmax, vmin);
     const float scale = span > 0.0f ? __fdiv_rn(static_cast<float>(NB), span) : 0.0f;
-    auto bin_of_key = [&](uint32_t key) {
-        const int q = __float2int_rz(__fmul_rn(__fsub_rn(key_value<DT>(key), vmin), scale));
-        return static_cast<uint32_t>(q < 0 ? 0 : (q > NB - 1 ? NB - 1 : q));
-    };
+    const float amax = fmaxf(fabsf(vmin), fabsf(vmax));
     // block-uniform from here on
-    bool by_keys = !(span > 0.0f && span <= kFltMax && scale > 0.0f && scale <= kFltMax);
+    bool by_keys = !(span > 0.0f && span <= kFltMax && scale > 0.0f && scale <= kFltMax &&
+                     span >= amax * (1.0f / 256.0f));
     uint32_t t = 0;
     if (!by_keys) {
 #pragma unroll
         for (int j = 0; j < NB / NT; ++j) hist[threadIdx.x + j * NT] = 0;
-        if (threadIdx.x == 0) {
-            c.bcast[0] = 0xFFFFFFFFu;  // smallest key of the r-th's bin
-            c.bcast[1] = 0u;           // largest key of the e-th's bin
-        }
         __syncthreads();
 #pragma unroll
-        for (int j = 0; j < ThreadKeys::kMax; ++j)
-            if (j < tk.count) atomicAdd(&hist[bin_of_key(tk.key[j])], 1u);
+        for (int j = 0; j < ThreadKeys::kMax; ++j) {
+            if (j < tk.count) {
+                const int q = __float2int_rz(__fmul_rn(__fsub_rn(key_value<DT>(tk.key[j]), vmin), scale));
+                atomicAdd(&hist[q < 0 ? 0 : (q > NB - 1 ? NB - 1 : q)], 1u);
+            }
+        }
         __syncthreads();
         if (threadIdx.x == 0) GBTOPK_TRACE_SET(blockIdx.x, 16, -1);  // (row kernel blocks)
         warp_find_two_bins<NB>(hist, e, r, c);
@@ -1088,18 +1103,12 @@ __device__ uint32_t value_threshold(const ThreadKeys &tk, uint32_t r, uint32_t e
         const uint32_t lim = r / 8u > 16u ? r / 8u : 16u;
         by_keys = c.bcast[7] > lim;
         if (!by_keys) {
-#pragma unroll
-            for (int j = 0; j < ThreadKeys::kMax; ++j) {
-                if (j < tk.count) {
-                    const uint32_t q = bin_of_key(tk.key[j]);
-                    if (q == b) atomicMin(&c.bcast[0], tk.key[j]);
-                    if (q == be) atomicMax(&c.bcast[1], tk.key[j]);
-                }
-            }
-            __syncthreads();
-            if (threadIdx.x == 0) GBTOPK_TRACE_SET(blockIdx.x, 18, -1);
-            upper_e = c.bcast[1];
-            t = c.bcast[0];
+            const float bw = span * (1.0f / static_cast<float>(NB));  // bin width
+            t = key_of_value<DT>(vmin + (static_cast<float>(b) - 0.5f) * bw, false);
+            if (t < kmin) t = kmin;
+            uint32_t u = key_of_value<DT>(vmin + (static_cast<float>(be) + 1.0f) * bw, true);
+            if (u > kmax) u = kmax;
+            upper_e = u > t ? u : t;
         }
     }
     if (by_keys) t = adaptive_threshold<NT, NB>(tk, r, e, kmin, kmax, hist, c, upper_e);
