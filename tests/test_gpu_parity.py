@@ -185,6 +185,36 @@ def test_ties_and_specials(dev, dtype, W, det):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("W", [20000, 50000])
+def test_guess_value_ranges(dev, dtype, W):
+    """Split rows whose sample ranges steer the threshold guess down each of
+    its branches: a range narrow against its magnitude (the key-width
+    search), a dense cluster beside a few huge outliers (a crowded value
+    bin), two clusters far apart, a range reaching both signs' largest
+    finite values (an infinite span) and plain normal rows (the value bins);
+    every result compared with the oracle."""
+    g = torch.Generator().manual_seed(31 + W)
+    fmax = {torch.float32: 3.0e38, torch.bfloat16: 3.0e38, torch.float16: 60000.0}[dtype]
+    rows = []
+    rows.append(1000.0 + torch.randn(W, generator=g) * 1e-2)              # narrow, far from zero
+    r = torch.randn(W, generator=g)
+    r[::1009] = fmax / 4                                                 # dense cluster + outliers
+    rows.append(r)
+    r = torch.randn(W, generator=g)
+    r[1::3] += 500.0                                                     # two far clusters
+    rows.append(r)
+    r = torch.randn(W, generator=g)
+    r[5::4001] = fmax
+    r[7::4001] = -fmax                                                   # span past the largest float
+    rows.append(r)
+    rows.append(torch.randn(W, generator=g))                             # plain
+    seq = [W] * len(rows)
+    for k in (64, 2048):
+        run_case(dev, _custom(rows, seq, k, dtype), det=False)
+        run_case(dev, _custom(rows, seq, k, dtype), det=True)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("W", [33, 512, 1000, 2048])
 def test_small_rows_warp_path(dev, dtype, W):
     """Widths up to 2048 without the deterministic order take the one-warp-per-row
